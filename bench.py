@@ -1,0 +1,427 @@
+"""Benchmark of the fake-quant hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload grouped_nvfp4|nvfp4_wa|int4_fp8|observer_fp8|int8_channel]
+
+One step = one pass of the workload's whole hot path: for the default
+workload (grouped NVFP4 MoE expert stacks, gate_up [128,1536,2048] + down
+[128,2048,768]) the vectorised QDQ forward of both stacks and the per-block
+scale gradient of both stacks, through the C ABI.  Inputs are resident in
+HBM and larger than L2.  Prints one JSON line (rank 0).
+
+Metric: algorithmic HBM bytes moved per second (GB/s), with elements/s and
+the fraction of the measured HBM copy bandwidth.  Under torchrun each rank
+runs the same workload on its own GPU (independent replicas, weak scaling);
+the time is the max over ranks.
+
+--impl reference times the CPU oracle (the plain double-precision
+implementation) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="grouped_nvfp4")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------
+# peaks, clocks, profile summaries
+# ---------------------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    """Hash of the CUDA sources: a stored ncu traffic figure is valid only for it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "learnable_scale_fake_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, if the
+    summary was taken on the current sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    digest = source_digest()
+    for line in open(p):
+        tok = line.strip().strip("|").split("|")
+        tok = [t.strip() for t in tok]
+        if len(tok) >= 3 and tok[0] == kernel and tok[2] == digest:
+            try:
+                return int(tok[1])
+            except ValueError:
+                return None
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 6]
+        os.unlink(self.file.name)
+        if not rows:
+            return {"samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" == r[3 + i].strip()})
+        try:
+            smax = float(rows[0][1])
+        except ValueError:
+            smax = None
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------
+
+def _oracle_jobs(name, inputs):
+    """(label, x, dy, oracle spec, rows per unit) for the workload's tensors;
+    x / dy are [units, ...] so that a sample is a leading slice."""
+    import oracle as O
+
+    def flat(t):
+        return t.reshape(-1, t.shape[-1])
+
+    if name == "grouped_nvfp4":
+        sp = O.spec(O.NVFP4, O.PER_GROUP, group=16)
+        return [(nm, inputs[nm], inputs[f"dy_{nm}"], sp) for nm in ("gate_up", "down")], "experts"
+    if name == "int4_fp8":
+        return [("stack", inputs["stack"], inputs["dy_stack"],
+                 O.spec(O.INT4, O.PER_GROUP, group=128, qmin=-8, qmax=7)),
+                ("dense", flat(inputs["dense"]).reshape(-1, 64, 8192),
+                 flat(inputs["dy_dense"]).reshape(-1, 64, 8192),
+                 O.spec(O.FP8_E4M3, O.PER_CHANNEL))], "leading units (expert / 64 rows)"
+    if name == "nvfp4_wa":
+        return [("w", flat(inputs["w"]).reshape(-1, 64, 4096), flat(inputs["dy_w"]).reshape(-1, 64, 4096),
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16)),
+                ("a", flat(inputs["a"]).reshape(-1, 64, 4096), flat(inputs["dy_a"]).reshape(-1, 64, 4096),
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK))], \
+            "leading units of 64 rows"
+    if name == "int8_channel":
+        return [("w", flat(inputs["w"]).reshape(-1, 16, 512), flat(inputs["dy"]).reshape(-1, 16, 512),
+                 O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127))], "leading units of 16 rows"
+    return [("act", inputs["act"], None, None)], "leading tokens"
+
+
+def oracle_run(name, inputs, k):
+    """The oracle, as it stands, on the first k units of each tensor (forward +
+    scale gradient; observer + scale + per-head QDQ for the observer workload).
+    Returns (algorithmic bytes, elements, seconds)."""
+    import oracle as O
+    from learnable_scale_fake_gb300 import synth
+
+    jobs, _ = _oracle_jobs(name, inputs)
+    nbytes = elems = 0
+    secs = 0.0
+    for nm, x, dy, sp in jobs:
+        kk = min(k, x.shape[0])
+        xb = synth.bf16_bits(x[:kk])
+        if sp is None:  # observer + scale + per-head E4M3 QDQ
+            t0 = time.perf_counter()
+            lo, hi = O.observer_minmax(xb)
+            sc = O.minmax_scale(lo, hi, 448.0)
+            O.qdq_fwd(O.spec(O.FP8_E4M3, O.PER_HEAD), xb, sc)
+            secs += time.perf_counter() - t0
+            nbytes += 6 * xb.size
+            elems += 2 * xb.size
+            continue
+        db = synth.bf16_bits(dy[:kk])
+        if xb.ndim == 2:
+            xb, db = xb[None], db[None]
+        s, ts = O.scale_init(sp, xb)  # the oracle's own scale init, untimed
+        t0 = time.perf_counter()
+        O.qdq_fwd(sp, xb, s, ts)
+        O.scale_grad(sp, xb, db, s, ts)
+        secs += time.perf_counter() - t0
+        m = xb.size
+        elems += 2 * m
+        nbytes += int(m * (8.75 if (sp.fmt == O.NVFP4 and sp.mode == O.SCALE_LEARNED) else 8.0))
+    return int(nbytes), elems, secs
+
+
+def oracle_pick(name, inputs, budget_s):
+    """Grows the sample (x4) until one oracle pass takes about budget_s / 4."""
+    jobs, unit = _oracle_jobs(name, inputs)
+    limit = min(j[1].shape[0] for j in jobs)
+    k = 1
+    while True:
+        res = oracle_run(name, inputs, k)
+        if res[2] > budget_s / 4 or k >= limit:
+            return k, res, f"first {k} {unit} of each tensor"
+        k = min(limit, k * 4)
+
+
+def reference_arm(args):
+    """--impl reference: the oracle, as it stands, on the host cores.  Inputs come
+    from the seeded generators directly; nothing of the CUDA library runs."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    from learnable_scale_fake_gb300 import synth
+
+    gen = {"grouped_nvfp4": lambda: synth.cfg3("cpu", 0, experts=4), "nvfp4_wa": lambda: synth.cfg2("cpu"),
+           "int4_fp8": lambda: synth.cfg4("cpu"), "int8_channel": lambda: synth.cfg1("cpu"),
+           "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)}}
+    inputs = gen[args.workload]()
+    k, _, desc = oracle_pick(args.workload, inputs, budget_s=4.0)
+    runs = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_run(args.workload, inputs, k)
+        if i >= args.warmup:
+            runs.append(r)
+    tb = sum(r[0] for r in runs)
+    ts = sum(r[2] for r in runs)
+    value = tb / ts / 1e9
+    threads = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": "fake-quant fwd+scale-grad algorithmic HBM GB/s",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * ts / len(runs), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": desc + ", fwd + scale grad"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+
+def max_over_ranks(value, dist, device):
+    import torch
+
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+
+    from learnable_scale_fake_gb300 import _build, aqfq, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    aqfq.lib()
+
+    wl = workloads.BUILDERS[args.workload](device)
+    stream = torch.cuda.Stream(device)
+    small = wl.bytes_per_step < 1.5 * 129e6
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if small else None
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            wl.step(stream)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, events per op and around the whole region ----
+    nops = len(wl.ops)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nops)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for k in range(args.steps):
+            if flush is not None:
+                flush.fill_(k & 0xFF)
+            for i, op in enumerate(wl.ops):
+                ev[k][i][0].record(stream)
+                op.run(stream)
+                ev[k][i][1].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    per_op = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
+              for i in range(nops)]
+    op_ms = [sum(v) / len(v) for v in per_op]
+    region_ms = t0.elapsed_time(t1)
+    step_ms = (sum(op_ms) if flush is not None else region_ms / args.steps)
+    step_ms = max_over_ranks(step_ms, dist, device)
+
+    bytes_step = wl.bytes_per_step
+    value = world * bytes_step / (step_ms * 1e-3) / 1e9
+    gelem = world * wl.elems_per_step / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    dom = max(range(nops), key=lambda i: op_ms[i])
+    dom_op = wl.ops[dom]
+    achieved = dom_op.bytes / (op_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom_op.kernel, "op": dom_op.name,
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
+            if peak_kind == "measured" else "fallback",
+            "traffic": stored_traffic(dom_op.kernel),
+            "algorithmic_bytes_per_launch": dom_op.bytes}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                   for k, v in wl.inputs.items()}
+        for k, v in wl.inputs.items():
+            host_in[k].copy_(v)
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                    for k, v in wl.outputs.items()}
+        bi = sum(v.numel() * v.element_size() for v in host_in.values())
+        bo = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in wl.inputs.items():
+                v.copy_(host_in[k], non_blocking=True)
+            wl.step(stream)
+            for k, v in wl.outputs.items():
+                host_out[k].copy_(v, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        with torch.cuda.stream(stream):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, device)
+        e2e = {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+               "steps": n_e2e}
+
+    # ---- CPU oracle on a bounded sample (rank 0, one GPU) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        k, _, desc = oracle_pick(args.workload, wl.inputs, budget_s=8.0)
+        nbytes, elems, secs = oracle_run(args.workload, wl.inputs, k)
+        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+               "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": desc + ", fwd + scale grad", "seconds": round(secs, 2),
+               "gelem_per_s": round(elems / secs / 1e9, 5)}
+
+    if rank == 0:
+        line = {
+            "metric": "fake-quant fwd+scale-grad algorithmic HBM GB/s", "value": round(value, 1),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "storage": "bf16", "data": "synthetic",
+            "config": dict(wl.config, l2=("flushed between steps (256 MiB write)" if small
+                                          else "inputs larger than L2"),
+                           parallelism=f"replicas x{world}"),
+            "gelem_per_s": round(gelem, 2),
+            "pct_hbm_measured": round(100 * value / world / peak, 1),
+            "pct_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+            "per_op_ms": {op.name: round(op_ms[i], 4) for i, op in enumerate(wl.ops)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * sum(op.launches for op in wl.ops),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

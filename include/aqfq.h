@@ -1,0 +1,206 @@
+/*
+ * aqfq.h -- C ABI of libaqfq: learnable-scale fake-quant (quantize-dequantize)
+ * of frozen BF16 weights and activations on one NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute (the method, restated from the pages):
+ *   - AngelSlim mcore_qad article, section 1: weights stay frozen in BF16; in
+ *     the forward pass weights and activations are quantized then dequantized
+ *     (fake-quant); the quantizer scales are the only trainable tensors.
+ *   - Same article, section 2.3: weight fake-quant is applied transparently to
+ *     module.weight, activations are fake-quantized before the matmul, the
+ *     gradient flows to the scales; router and output layer are not quantized
+ *     (callers simply do not pass them here).
+ *   - Same article, section 2.4: each MoE layer's experts become one 3D stack
+ *     [E, N, K] that is fake-quantized in one vectorised pass.
+ *   - Same article, section 3: formats nvfp4, nvfp4a16, w4a16 (INT4), w8a8
+ *     (INT8), fp8; section 6: scale sources learnable / dynamic / calibrated.
+ *   - "QAT + DeepSpeed ZeRO-3" (AngelSlim docs), "Quantizer changes": the
+ *     fake-quant output is cast back to the input dtype (BF16 in, BF16 out);
+ *     "Quantizer initial values": a PTQ weight scale is about max|W|/448.
+ *   - msModelSlim "multi-card quantization adaptation guide", "FA3Quant"
+ *     steps 3-4: per-head min/max observer with a running merge; qparams are
+ *     computed from the merged min/max.
+ *
+ * Arithmetic (identical for every format; all binary32, round to nearest even):
+ *   v     = x / s                (IEEE division; s = 0 gives v = +-0, sign of x)
+ *   q     = grid(v)              nearest grid value, ties to the even code,
+ *                                saturating at the grid's ends
+ *   x_hat = bf16(q * s)          product rounded to binary32, then to BF16
+ *   grid: INT8/INT4 integers in [qmin, qmax] (integer 0 has no sign);
+ *         FP8 E4M3 (largest 448); NVFP4 E2M1 (largest 6), sign of zero kept.
+ *   NVFP4 block scale: e_b = E4M3(S_b / g) (saturating), s = dec(e_b) * g.
+ *   Scale gradient (straight-through estimator, LSQ form):
+ *         d x_hat / d s = q - v if the clamp is inactive, q if it is active
+ *         (INT: v <= qmin or v >= qmax; FP: |v| >= largest finite value);
+ *         d x_hat / d x = 1 if inactive, 0 if active.
+ *
+ * Layouts (all row-major, K contiguous, BF16 as 16-bit patterns):
+ *   x, y, dy, dx : [batch, rows, K]   (batch = experts E for stacks, else 1;
+ *                                      [T, H, D] for per-head activations)
+ *   scale        : AQFQ_PER_TENSOR [batch]; AQFQ_PER_CHANNEL [batch, rows];
+ *                  AQFQ_PER_GROUP [batch, rows, K/group]; AQFQ_PER_HEAD [rows]
+ *                  (shared by all batch entries); NVFP4 learned [batch, rows, K/16]
+ *   tensor_scale : NVFP4 only, [batch] float
+ *   codes        : optional; INT8 / FP8: one byte per element [batch, rows, K];
+ *                  INT4 / NVFP4: two per byte [batch, rows, K/2], element k even
+ *                  in the low nibble (INT4 nibbles are two's complement,
+ *                  E2M1 nibbles are sign<<3 | exponent<<1 | mantissa)
+ *   block_codes  : optional, NVFP4 only: E4M3 byte per block [batch, rows, K/16]
+ *
+ * Ownership and errors: every pointer is device memory owned by the caller;
+ * the library allocates nothing and keeps no state between calls (it caches
+ * the SM count of each device).  Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*, NULL = legacy default stream) and never
+ * synchronise.  Arguments are checked on the host before anything is
+ * launched; a rejected call launches nothing and returns a status:
+ *   AQFQ_ERR_NULL         a required pointer is NULL (a buffer with no
+ *                         elements may be NULL)
+ *   AQFQ_ERR_SHAPE        negative size, K % 16 != 0, K % group != 0, or a
+ *                         size beyond the limits stated per call
+ *   AQFQ_ERR_ALIGN        x / y / dy / dx not 32-byte aligned; codes not
+ *                         8-byte (packed) or 16-byte (byte codes) aligned;
+ *                         float arrays not 4-byte aligned; workspace not 8-byte
+ *   AQFQ_ERR_UNSUPPORTED  a format / granularity / mode combination the
+ *                         library does not implement
+ *   AQFQ_ERR_WORKSPACE    workspace smaller than aqfq_scale_grad_workspace_bytes
+ *   AQFQ_ERR_CUDA         a launch failed (cudaGetLastError after launching)
+ * Inputs are assumed finite (no NaN / Inf); the library does not check them.
+ */
+#ifndef AQFQ_H
+#define AQFQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum aqfq_status {
+  AQFQ_OK = 0,
+  AQFQ_ERR_NULL = 1,
+  AQFQ_ERR_SHAPE = 2,
+  AQFQ_ERR_ALIGN = 3,
+  AQFQ_ERR_UNSUPPORTED = 4,
+  AQFQ_ERR_WORKSPACE = 5,
+  AQFQ_ERR_CUDA = 6
+} aqfq_status;
+
+/* element formats (AngelSlim mcore_qad article, section 3) */
+enum { AQFQ_INT8 = 0, AQFQ_INT4 = 1, AQFQ_FP8_E4M3 = 2, AQFQ_NVFP4 = 3 };
+/* scale granularities */
+enum { AQFQ_PER_TENSOR = 0, AQFQ_PER_CHANNEL = 1, AQFQ_PER_GROUP = 2, AQFQ_PER_HEAD = 3 };
+/* scale sources (same article, section 6: learnable / dynamic) */
+enum { AQFQ_SCALE_LEARNED = 0, AQFQ_SCALE_DYNAMIC_BLOCK = 1 };
+
+/* Quantizer description.
+ *   fmt   : AQFQ_INT8 | AQFQ_INT4 | AQFQ_FP8_E4M3 | AQFQ_NVFP4
+ *   gran  : AQFQ_PER_*; NVFP4 requires AQFQ_PER_GROUP with group 16
+ *   group : elements per scale along K for AQFQ_PER_GROUP: a power of two in
+ *           [16, 512] (128 for w4a16 INT4), ignored otherwise
+ *   qmin, qmax : integer grid for INT8 (within [-128, 127]) and INT4 (within
+ *           [-8, 7]), qmin < 0 < qmax; ignored for FP8 / NVFP4
+ *   mode  : AQFQ_SCALE_LEARNED (scale given by the caller), or, NVFP4 only,
+ *           AQFQ_SCALE_DYNAMIC_BLOCK: block scale S_b = amax_b / 6 computed
+ *           from the data, the tensor scale g is the learned one. */
+typedef struct aqfq_qspec {
+  int32_t fmt;
+  int32_t gran;
+  int32_t group;
+  int32_t qmin;
+  int32_t qmax;
+  int32_t mode;
+} aqfq_qspec;
+
+/* Fake-quant forward: y = x_hat (BF16, same shape as x) and, if non-NULL, the
+ * packed codes and (NVFP4) the E4M3 block codes.
+ * Source: AngelSlim mcore_qad article, sections 1 and 2.3 (weights and
+ * activations quantized-dequantized in the forward), section 3 (formats);
+ * "QAT + DeepSpeed ZeRO-3", "Quantizer changes" (output cast back to BF16).
+ *   x            device, [batch, rows, K] BF16
+ *   scale        device, shaped by spec->gran (NULL only for NVFP4 dynamic)
+ *   tensor_scale device, [batch] float (NVFP4), else ignored
+ *   y            device, [batch, rows, K] BF16; must not overlap x
+ * Limits: rows * K / 16 < 2^32 (per batch entry). */
+aqfq_status aqfq_qdq_fwd(const aqfq_qspec* spec, const void* x, int64_t batch, int64_t rows,
+                         int64_t K, const float* scale, const float* tensor_scale, void* y,
+                         uint8_t* codes, uint8_t* block_codes, void* stream);
+
+/* The same forward over a 3D stack of MoE expert weights w [E, N, K]: one
+ * vectorised pass over every expert, per-expert tensor scale (NVFP4).
+ * Source: AngelSlim mcore_qad article, section 2.4 (3D stacked expert
+ * weights, whole-stack vectorised fake-quant, then one grouped GEMM).
+ * Arguments as aqfq_qdq_fwd with batch = E, rows = N. */
+aqfq_status aqfq_grouped_qdq(const aqfq_qspec* spec, const void* w, int64_t E, int64_t N,
+                             int64_t K, const float* scale, const float* tensor_scale, void* y,
+                             uint8_t* codes, uint8_t* block_codes, void* stream);
+
+/* Straight-through scale gradient: dscale = sum over each scale's unit of
+ * dy * (d x_hat / d s); optional STE input gradient dx = dy where the clamp
+ * is inactive, +0 where active.  Weights are frozen, so callers pass dx =
+ * NULL for weights.
+ * Source: AngelSlim mcore_qad article, section 1 (only the scales are
+ * optimised) and 2.3 (the gradient flows to the scale through the fake-quant).
+ *   dy            device, [batch, rows, K] BF16, upstream gradient dL/dx_hat
+ *   dscale        device, shaped like scale; learned modes only (NULL for
+ *                 NVFP4 dynamic)
+ *   dtensor_scale device, [batch] float: NVFP4 dynamic mode only (gradient of
+ *                 the learned tensor scale with the block codes held fixed);
+ *                 must be NULL otherwise
+ *   dx            device, optional, [batch, rows, K] BF16
+ *   accumulate    0: overwrite dscale / dtensor_scale; else add to them
+ *   workspace     device scratch, >= aqfq_scale_grad_workspace_bytes(...)
+ *                 bytes (0 bytes for per-channel / per-group / NVFP4 learned;
+ *                 the result is deterministic: fixed reduction order)
+ * Not implemented: AQFQ_PER_HEAD (AQFQ_ERR_UNSUPPORTED). */
+aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
+                            int64_t rows, int64_t K, const float* scale,
+                            const float* tensor_scale, float* dscale, float* dtensor_scale,
+                            void* dx, int accumulate, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Bytes of device scratch aqfq_scale_grad needs for these arguments (0 when
+ * none); returns 0 for arguments aqfq_scale_grad would reject. */
+size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, int64_t rows,
+                                       int64_t K);
+
+/* Per-head min/max observer over x [T, H, D] (BF16): min_out[h] / max_out[h]
+ * = min / max of x[:, h, :] (exact BF16 values as float; -0 orders below +0).
+ * accumulate != 0 merges with the values already in min_out / max_out (the
+ * running min/max of successive calibration batches; merging shards this way
+ * equals one pass over all of them).  With T = 0 and accumulate = 0 the
+ * result is +inf / -inf.
+ * Source: msModelSlim guide, "FA3Quant" steps 3-4 (per-head local min/max,
+ * min-of-mins / max-of-maxes merge).
+ * Limits: D % 16 == 0; H * D / 16 <= 2^24. */
+aqfq_status aqfq_observer_minmax(const void* x, int64_t T, int64_t H, int64_t D, float* min_out,
+                                 float* max_out, int accumulate, void* stream);
+
+/* Per-head symmetric scale from the observer: scale[h] = max(|min|, |max|) /
+ * qmax (binary32 division; qmax = 448 for E4M3).  The result feeds
+ * aqfq_qdq_fwd with gran = AQFQ_PER_HEAD.
+ * Source: msModelSlim guide, "FA3Quant" step 3 (qparams from the merged
+ * min/max); "QAT + DeepSpeed ZeRO-3", "Quantizer initial values" (amax/448). */
+aqfq_status aqfq_minmax_scale(const float* min_in, const float* max_in, int64_t H, float qmax,
+                              float* scale_out, void* stream);
+
+/* Scale initialisation from the data: every scale = amax over its unit /
+ * qmax (INT: spec->qmax; FP8: 448).  NVFP4 learned: scale = amax_b / 6 per
+ * 16-element block and tensor_scale[b] = amax / (448 * 6) per batch entry;
+ * NVFP4 dynamic: tensor_scale only (scale may be NULL).
+ * Source: "QAT + DeepSpeed ZeRO-3", "Quantizer initial values" (PTQ scale
+ * about max|W| / 448); the INT8 rule amax / 127 is the same rule on the
+ * integer grid. */
+aqfq_status aqfq_scale_init(const aqfq_qspec* spec, const void* x, int64_t batch, int64_t rows,
+                            int64_t K, float* scale, float* tensor_scale, void* stream);
+
+/* Static text for a status code. */
+const char* aqfq_status_string(aqfq_status status);
+
+/* ABI version (major * 100 + minor). */
+int aqfq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AQFQ_H */

@@ -1,0 +1,272 @@
+// aqfq_device.cuh -- device-side building blocks of libaqfq (sm_103a).
+//
+// One "chunk" is 16 consecutive BF16 elements along K (32 bytes): one 256-bit
+// load per operand, one NVFP4 block, 1/8 of an INT4 g128 group.  Every kernel
+// maps one lane to one chunk at a time, so loads are perfectly coalesced
+// (a warp streams 1 KiB contiguous per operand) and an NVFP4 block's amax and
+// gradient sum never leave the lane.
+//
+// Rounding steps follow the library's contract (include/aqfq.h):
+//   v = x / s        IEEE binary32 division (__fdiv_rn; built without fast math)
+//   q = grid(v)      integer grid: clamp then round-half-even by the 1.5*2^23
+//                    addition trick (exact for |v| < 2^22); E4M3 / E2M1: the
+//                    hardware cvt.rn.satfinite conversions
+//   x_hat = bf16(q*s) __fmul_rn (never contracted into an FMA), cvt.rn.bf16x2
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace aqfq {
+
+constexpr int kThreads = 256;  // threads per CTA for every streaming kernel
+constexpr int kChunk = 16;     // elements per lane-chunk
+
+enum Fmt { F_INT8 = 0, F_INT4 = 1, F_FP8 = 2, F_NVFP4 = 3 };
+enum Gran { G_TENSOR = 0, G_ROW = 1, G_GROUP = 2, G_HEAD = 3 };
+
+// ---------------------------------------------------------------------------
+// n / d for 32-bit n by multiply-high and shifts (Granlund & Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994, Fig. 4.1).
+// ---------------------------------------------------------------------------
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;  // l = ceil(log2 d)
+  f.m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 1 ? l - 1 : 0;
+  return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
+// ---------------------------------------------------------------------------
+// 256-bit streaming memory access (sm_100+ vector width)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ld_stream(const void* p, uint32_t (&w)[8]) {
+  asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+        "=r"(w[7])
+      : "l"(p));
+}
+
+__device__ __forceinline__ void st_256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_64(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// BF16 <-> binary32
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// two binary32 values -> packed BF16 pair, round to nearest even (hi in bits 31..16)
+__device__ __forceinline__ uint32_t pack_bf16x2(float hi, float lo) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float sign_zero(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 and E2M1 conversions (PTX cvt, saturating to the largest finite value)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float h2f(uint16_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+
+// packed E4M3 pair (element in bits 7..0 -> .x) -> two binary32 values (exact)
+__device__ __forceinline__ float2 dec_e4m3x2(uint32_t c) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
+  return make_float2(h2f((uint16_t)(h & 0xFFFF)), h2f((uint16_t)(h >> 16)));
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 t, z;\n\t"
+      "mov.b16 {t, z}, 0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "mov.b32 %0, {t, z, z, z}; }"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// packed E2M1 pair (element in bits 3..0 -> .x) -> two binary32 values (exact)
+__device__ __forceinline__ float2 dec_e2m1x2(uint32_t c) {
+  uint32_t h;
+  asm("{ .reg .b8 t, u, v, w;\n\t"
+      "mov.b32 {t, u, v, w}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t; }"
+      : "=r"(h)
+      : "r"(c));
+  return make_float2(h2f((uint16_t)(h & 0xFFFF)), h2f((uint16_t)(h >> 16)));
+}
+
+// ---------------------------------------------------------------------------
+// Element grids.  quant_pair rounds (v0, v1) = elements (2i, 2i+1) of a chunk
+// and returns the grid values, the packed codes of the pair and whether the
+// clamp is active for each (the gradient's switch).
+// ---------------------------------------------------------------------------
+struct IntRange {
+  float qmin, qmax;
+};
+
+// clamp then round half to even via t = vc + 1.5*2^23 (|vc| <= 128 << 2^22):
+// t's low bits hold the integer in two's complement; t - 1.5*2^23 is the
+// integer as +0 for zero (an integer code carries no sign).
+__device__ __forceinline__ float int_round(float v, const IntRange& r, uint32_t& code) {
+  const float kMagic = 12582912.0f;  // 1.5 * 2^23
+  float vc = fminf(fmaxf(v, r.qmin), r.qmax);
+  float t = __fadd_rn(vc, kMagic);
+  code = __float_as_uint(t);
+  return __fsub_rn(t, kMagic);
+}
+
+template <int FMT>
+__device__ __forceinline__ void quant_pair(float v0, float v1, const IntRange& r, float& q0,
+                                           float& q1, uint32_t& code, bool& k0, bool& k1) {
+  if constexpr (FMT == F_INT8 || FMT == F_INT4) {
+    uint32_t c0, c1;
+    q0 = int_round(v0, r, c0);
+    q1 = int_round(v1, r, c1);
+    if constexpr (FMT == F_INT8) code = (c0 & 0xFFu) | ((c1 & 0xFFu) << 8);
+    else code = (c0 & 0xFu) | ((c1 & 0xFu) << 4);
+    k0 = (v0 <= r.qmin) || (v0 >= r.qmax);
+    k1 = (v1 <= r.qmin) || (v1 >= r.qmax);
+  } else if constexpr (FMT == F_FP8) {
+    code = cvt_e4m3x2(v1, v0);
+    float2 d = dec_e4m3x2(code);
+    q0 = d.x;
+    q1 = d.y;
+    k0 = fabsf(v0) >= 448.0f;
+    k1 = fabsf(v1) >= 448.0f;
+  } else {
+    code = cvt_e2m1x2(v1, v0);
+    float2 d = dec_e2m1x2(code);
+    q0 = d.x;
+    q1 = d.y;
+    k0 = fabsf(v0) >= 6.0f;
+    k1 = fabsf(v1) >= 6.0f;
+  }
+}
+
+// bits of the packed codes of one chunk: INT8/FP8 one byte per element (16 B),
+// INT4/NVFP4 one nibble per element (8 B)
+template <int FMT>
+__device__ __forceinline__ void put_code(uint32_t (&cw)[4], int pair, uint32_t code) {
+  if constexpr (FMT == F_INT8 || FMT == F_FP8) {
+    cw[pair >> 1] |= code << (16 * (pair & 1));
+  } else {
+    cw[pair >> 2] |= code << (8 * (pair & 3));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 block scale: e = E4M3(S_b / g) (saturating), S_hat = dec(e) * g
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float nvfp4_block_scale(float sb, float g, uint32_t& ecode) {
+  float r = (g != 0.0f) ? __fdiv_rn(sb, g) : 0.0f;
+  ecode = cvt_e4m3x2(0.0f, r) & 0xFFu;
+  return __fmul_rn(dec_e4m3x2(ecode).x, g);
+}
+
+// largest |x| of a chunk as binary32 (exact: a BF16 value)
+__device__ __forceinline__ float chunk_amax(const uint32_t (&w)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  uint32_t a = max(m & 0xFFFFu, m >> 16);
+  return __uint_as_float(a << 16);
+}
+
+// ---------------------------------------------------------------------------
+// One chunk, forward: y = bf16(q * s), packed codes
+// ---------------------------------------------------------------------------
+template <int FMT, bool CODES>
+__device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[8], float s, const IntRange& r,
+                                          uint32_t (&yw)[8], uint32_t (&cw)[4]) {
+  if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
+  const bool zero = (s == 0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x0 = bf_lo(xw[i]), x1 = bf_hi(xw[i]);
+    const float v0 = zero ? sign_zero(x0) : __fdiv_rn(x0, s);
+    const float v1 = zero ? sign_zero(x1) : __fdiv_rn(x1, s);
+    float q0, q1;
+    uint32_t code;
+    bool k0, k1;
+    quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
+    yw[i] = pack_bf16x2(__fmul_rn(q1, s), __fmul_rn(q0, s));
+    if (CODES) put_code<FMT>(cw, i, code);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One chunk, backward: returns sum_i dy_i * (clamped ? q_i : q_i - v_i), summed
+// pairwise in a fixed tree; optional STE mask of dy.  The term q - v is exact
+// in binary32 (q and v are within a factor of two, Sterbenz), so the only
+// roundings are one per product and four levels of the tree.
+// ---------------------------------------------------------------------------
+template <int FMT, bool DX>
+__device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[8], const uint32_t (&dw)[8],
+                                            float s, const IntRange& r, uint32_t (&dxw)[8]) {
+  float t[16];
+  const bool zero = (s == 0.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x0 = bf_lo(xw[i]), x1 = bf_hi(xw[i]);
+    const float v0 = zero ? sign_zero(x0) : __fdiv_rn(x0, s);
+    const float v1 = zero ? sign_zero(x1) : __fdiv_rn(x1, s);
+    float q0, q1;
+    uint32_t code;
+    bool k0, k1;
+    quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
+    const float term0 = k0 ? q0 : __fsub_rn(q0, v0);
+    const float term1 = k1 ? q1 : __fsub_rn(q1, v1);
+    t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
+    t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
+    if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
+  }
+#pragma unroll
+  for (int w = 1; w < 16; w *= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+  }
+  return t[0];
+}
+
+}  // namespace aqfq

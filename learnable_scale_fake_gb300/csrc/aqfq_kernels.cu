@@ -1,0 +1,436 @@
+// aqfq_kernels.cu -- fake-quant forward and straight-through scale gradient.
+//
+// Forward (every format and granularity): one streaming kernel.  A CTA of 256
+// threads covers 256*U consecutive 16-element chunks of one batch entry (one
+// expert of a stack, gridDim.y over entries); each lane issues its U 256-bit
+// loads (plus its scale) before computing, then writes one 256-bit BF16 chunk
+// and, on request, its packed codes.  No shared memory, no cross-lane traffic.
+// Source of the operation: AngelSlim mcore_qad article, sections 1, 2.3, 2.4
+// (whole-stack vectorised fake-quant) and 3 (formats).
+//
+// Gradient: the same chunk walk recomputes v and q exactly as the forward,
+// forms dy * (clamped ? q : q - v) per element and reduces it
+//   - per block / group (units of 16..512 elements = 1..32 aligned lanes):
+//     pairwise tree in the lane, xor-butterfly across the unit's lanes, one
+//     store per unit (no atomics, no workspace);
+//   - per channel with long rows: one warp per row, per-lane double
+//     accumulation of chunk sums, double butterfly;
+//   - per tensor / NVFP4 tensor scale: per-CTA double partials into the
+//     caller's workspace, then a one-warp-per-entry pass in fixed order.
+// Every order is fixed, so results are bit-reproducible run to run.
+#include "aqfq_internal.h"
+
+namespace aqfq {
+
+namespace {
+
+constexpr int kMaxParts = 1024;  // CTAs per batch entry for the cross-CTA reductions
+
+struct FwdArgs {
+  const uint8_t* x;
+  uint8_t* y;
+  const float* scale;
+  const float* tscale;
+  uint8_t* codes;
+  uint8_t* bcodes;
+  int64_t batch, rows;
+  uint32_t cpb;
+  FastDiv cpr;
+  int lg;
+  IntRange ir;
+};
+
+template <int FMT, int GRAN, bool DYN, bool CODES, int U>
+__global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
+  for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
+    const uint64_t base = (uint64_t)b * a.cpb;
+    float g = 0.0f, st = 0.0f;
+    if constexpr (FMT == F_NVFP4) g = __ldg(a.tscale + b);
+    if constexpr (GRAN == G_TENSOR) st = __ldg(a.scale + b);
+    for (uint64_t c0 = (uint64_t)blockIdx.x * (kThreads * U); c0 < a.cpb;
+         c0 += (uint64_t)gridDim.x * (kThreads * U)) {
+      uint32_t xw[U][8];
+      float sraw[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint64_t c = c0 + j * kThreads + threadIdx.x;
+        sraw[j] = st;
+        if (c < a.cpb) {
+          const uint64_t gc = base + c;
+          ld_stream(a.x + gc * 32, xw[j]);
+          if constexpr (FMT == F_NVFP4) {
+            if constexpr (!DYN) sraw[j] = __ldg(a.scale + gc);
+          } else if constexpr (GRAN == G_ROW) {
+            sraw[j] = __ldg(a.scale + b * a.rows + fdiv((uint32_t)c, a.cpr));
+          } else if constexpr (GRAN == G_HEAD) {
+            sraw[j] = __ldg(a.scale + fdiv((uint32_t)c, a.cpr));
+          } else if constexpr (GRAN == G_GROUP) {
+            sraw[j] = __ldg(a.scale + (gc >> a.lg));
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint64_t c = c0 + j * kThreads + threadIdx.x;
+        if (c >= a.cpb) continue;
+        const uint64_t gc = base + c;
+        float s = sraw[j];
+        uint32_t ecode = 0;
+        if constexpr (FMT == F_NVFP4) {
+          const float sb = DYN ? __fdiv_rn(chunk_amax(xw[j]), 6.0f) : sraw[j];
+          s = nvfp4_block_scale(sb, g, ecode);
+        }
+        uint32_t yw[8], cw[4];
+        qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
+        st_256(a.y + gc * 32, yw);
+        if constexpr (CODES) {
+          if constexpr (FMT == F_INT8 || FMT == F_FP8) {
+            st_128(a.codes + gc * 16, cw[0], cw[1], cw[2], cw[3]);
+          } else {
+            st_64(a.codes + gc * 8, cw[0], cw[1]);
+          }
+          if constexpr (FMT == F_NVFP4) a.bcodes[gc] = (uint8_t)ecode;
+        }
+      }
+    }
+  }
+}
+
+struct GradArgs {
+  const uint8_t* x;
+  const uint8_t* dy;
+  uint8_t* dx;
+  const float* scale;
+  const float* tscale;
+  float* dscale;
+  double* ws;
+  int64_t batch, rows;
+  uint32_t cpb;
+  FastDiv cpr;
+  int lg;
+  IntRange ir;
+  int accumulate;
+  int nparts;
+};
+
+__device__ __forceinline__ void store_grad(float* p, float g, int accumulate) {
+  *p = accumulate ? __fadd_rn(*p, g) : g;
+}
+
+// RED = 0: one scale per aligned run of (1 << lg) lanes, written directly.
+// RED = 1: one scale (or NVFP4 tensor scale) per batch entry, CTA partials.
+template <int FMT, int GRAN, bool DYN, bool DX, int RED, int U>
+__global__ void __launch_bounds__(kThreads) scale_grad_kernel(const GradArgs a) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
+    const uint64_t base = (uint64_t)b * a.cpb;
+    float g = 0.0f, st = 0.0f;
+    if constexpr (FMT == F_NVFP4) g = __ldg(a.tscale + b);
+    if constexpr (GRAN == G_TENSOR) st = __ldg(a.scale + b);
+    double acc = 0.0;
+    for (uint64_t c0 = (uint64_t)blockIdx.x * (kThreads * U); c0 < a.cpb;
+         c0 += (uint64_t)gridDim.x * (kThreads * U)) {
+      uint32_t xw[U][8], dw[U][8];
+      float sraw[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint64_t c = c0 + j * kThreads + threadIdx.x;
+        sraw[j] = st;
+        if (c < a.cpb) {
+          const uint64_t gc = base + c;
+          ld_stream(a.x + gc * 32, xw[j]);
+          ld_stream(a.dy + gc * 32, dw[j]);
+          if constexpr (GRAN == G_GROUP && !DYN) sraw[j] = __ldg(a.scale + (gc >> a.lg));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint64_t c = c0 + j * kThreads + threadIdx.x;
+        const bool valid = c < a.cpb;
+        const uint64_t gc = base + c;
+        float cs = 0.0f;
+        float dec = 1.0f;
+        if (valid) {
+          float s = sraw[j];
+          if constexpr (FMT == F_NVFP4) {
+            uint32_t ecode;
+            const float sb = DYN ? __fdiv_rn(chunk_amax(xw[j]), 6.0f) : sraw[j];
+            s = nvfp4_block_scale(sb, g, ecode);
+            dec = dec_e4m3x2(ecode).x;
+          }
+          uint32_t dxw[8];
+          cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          if constexpr (DX) st_256(a.dx + gc * 32, dxw);
+        }
+        if constexpr (RED == 0) {
+          const int width = 1 << a.lg;
+          for (int off = 1; off < width; off <<= 1)
+            cs = __fadd_rn(cs, __shfl_xor_sync(0xFFFFFFFFu, cs, off));
+          if (valid && (lane & (width - 1)) == 0) store_grad(a.dscale + (gc >> a.lg), cs, a.accumulate);
+        } else {
+          // NVFP4 dynamic: d S_hat / d g = dec(e_b) with the block code held fixed
+          acc += (double)cs * (double)dec;
+        }
+      }
+    }
+    if constexpr (RED == 1) {
+      __shared__ double red[kThreads / 32];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+      if (lane == 0) red[threadIdx.x >> 5] = acc;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+        a.ws[b * a.nparts + blockIdx.x] = t;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// per-channel gradient for rows whose K is not a power of two <= 512: one warp
+// per row, lanes stride over the row's chunks
+template <int FMT, bool DX, int U>
+__global__ void __launch_bounds__(kThreads) scale_grad_row_kernel(const GradArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = a.batch * a.rows;
+  const uint32_t cpr = a.cpr.d;
+  for (int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); row < nrows;
+       row += (int64_t)gridDim.x * (kThreads / 32)) {
+    const float s = __ldg(a.scale + row);
+    const uint64_t base = (uint64_t)row * cpr;
+    double acc = 0.0;
+    for (uint32_t c0 = 0; c0 < cpr; c0 += 32 * U) {
+      uint32_t xw[U][8], dw[U][8];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + j * 32 + lane;
+        if (c < cpr) {
+          ld_stream(a.x + (base + c) * 32, xw[j]);
+          ld_stream(a.dy + (base + c) * 32, dw[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + j * 32 + lane;
+        if (c < cpr) {
+          uint32_t dxw[8];
+          acc += (double)grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          if constexpr (DX) st_256(a.dx + (base + c) * 32, dxw);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (lane == 0) store_grad(a.dscale + row, (float)acc, a.accumulate);
+  }
+}
+
+// sum of the CTA partials of each batch entry, in a fixed order
+__global__ void reduce_partials_kernel(const double* ws, int nparts, int64_t batch, float* out,
+                                       int accumulate) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); b < batch;
+       b += (int64_t)gridDim.x * (blockDim.x / 32)) {
+    double t = 0.0;
+    for (int i = lane; i < nparts; i += 32) t += ws[b * nparts + i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+    if (lane == 0) store_grad(out + b, (float)t, accumulate);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host-side dispatch
+// ---------------------------------------------------------------------------
+
+int log2_exact(int64_t v) {
+  int l = 0;
+  while ((int64_t(1) << l) < v) ++l;
+  return (int64_t(1) << l) == v ? l : -1;
+}
+
+dim3 stream_grid(uint32_t cpb, int64_t batch, int U, int cap) {
+  uint64_t gx = (uint64_t(cpb) + uint64_t(kThreads) * U - 1) / (uint64_t(kThreads) * U);
+  if (gx < 1) gx = 1;
+  if (cap > 0 && gx > uint64_t(cap)) gx = cap;
+  if (gx > 0x7FFFFFFFull) gx = 0x7FFFFFFFull;
+  uint64_t gy = batch < 65535 ? uint64_t(batch) : 65535ull;
+  if (gy < 1) gy = 1;
+  return dim3((unsigned)gx, (unsigned)gy, 1);
+}
+
+template <int FMT, int GRAN, bool DYN, bool CODES>
+void fwd_launch(const FwdArgs& a, cudaStream_t st) {
+  if (a.cpb >= 2u * kThreads) {
+    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 2><<<stream_grid(a.cpb, a.batch, 2, 0), kThreads, 0, st>>>(a);
+  } else {
+    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 1><<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
+  }
+}
+
+template <int FMT, bool CODES>
+void fwd_gran(const Problem& p, const FwdArgs& a, cudaStream_t st) {
+  if constexpr (FMT == F_NVFP4) {
+    if (p.mode == 1) fwd_launch<FMT, G_GROUP, true, CODES>(a, st);
+    else fwd_launch<FMT, G_GROUP, false, CODES>(a, st);
+  } else {
+    switch (p.gran) {
+      case G_TENSOR: fwd_launch<FMT, G_TENSOR, false, CODES>(a, st); break;
+      case G_ROW: fwd_launch<FMT, G_ROW, false, CODES>(a, st); break;
+      case G_GROUP: fwd_launch<FMT, G_GROUP, false, CODES>(a, st); break;
+      default: fwd_launch<FMT, G_HEAD, false, CODES>(a, st); break;
+    }
+  }
+}
+
+template <int FMT>
+void fwd_codes(const Problem& p, const FwdArgs& a, cudaStream_t st) {
+  if (a.codes) fwd_gran<FMT, true>(p, a, st);
+  else fwd_gran<FMT, false>(p, a, st);
+}
+
+int grad_unroll(uint32_t cpb) { return cpb >= 2u * kThreads ? 2 : 1; }
+
+bool grad_needs_partials(const Problem& p) {
+  return (p.fmt == F_NVFP4 && p.mode == 1) || (p.fmt != F_NVFP4 && p.gran == G_TENSOR);
+}
+
+int grad_parts(const Problem& p) {
+  const int U = grad_unroll(p.cpb);
+  return (int)stream_grid(p.cpb, 1, U, kMaxParts).x;
+}
+
+// block-path lanes per unit (log2), or -1 when the row kernel is needed
+int grad_unit_lg(const Problem& p) {
+  if (p.fmt == F_NVFP4) return 0;
+  if (p.gran == G_GROUP) return log2_exact(p.group / 16);
+  if (p.gran == G_ROW) {
+    const int l = log2_exact(p.K / 16);
+    return (l >= 0 && l <= 5) ? l : -1;
+  }
+  return 0;
+}
+
+template <int FMT, int GRAN, bool DYN, bool DX, int RED>
+void grad_launch(const GradArgs& a, cudaStream_t st) {
+  if (grad_unroll(a.cpb) == 2) {
+    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 2>
+        <<<stream_grid(a.cpb, a.batch, 2, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
+  } else {
+    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>
+        <<<stream_grid(a.cpb, a.batch, 1, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
+  }
+}
+
+template <int FMT, bool DX>
+void grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
+  if constexpr (FMT == F_NVFP4) {
+    if (p.mode == 1) grad_launch<FMT, G_GROUP, true, DX, 1>(a, st);
+    else grad_launch<FMT, G_GROUP, false, DX, 0>(a, st);
+  } else {
+    if (p.gran == G_TENSOR) {
+      grad_launch<FMT, G_TENSOR, false, DX, 1>(a, st);
+    } else if (a.lg >= 0) {  // per-group, or per-channel rows of 16..512 (power of two)
+      grad_launch<FMT, G_GROUP, false, DX, 0>(a, st);
+    } else {
+      const int64_t nrows = p.batch * p.rows;
+      int64_t blocks = (nrows + kThreads / 32 - 1) / (kThreads / 32);
+      if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+      if (blocks < 1) blocks = 1;
+      scale_grad_row_kernel<FMT, DX, 2><<<(unsigned)blocks, kThreads, 0, st>>>(a);
+    }
+  }
+}
+
+template <int FMT>
+void grad_fmt(const Problem& p, const GradArgs& a, cudaStream_t st) {
+  if (a.dx) grad_dispatch<FMT, true>(p, a, st);
+  else grad_dispatch<FMT, false>(p, a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_qdq_fwd(const Problem& p, const void* x, const float* scale,
+                           const float* tscale, void* y, uint8_t* codes, uint8_t* bcodes,
+                           cudaStream_t st) {
+  if (p.batch == 0 || p.cpb == 0) return cudaSuccess;
+  FwdArgs a;
+  a.x = static_cast<const uint8_t*>(x);
+  a.y = static_cast<uint8_t*>(y);
+  a.scale = scale;
+  a.tscale = tscale;
+  a.codes = codes;
+  a.bcodes = bcodes;
+  a.batch = p.batch;
+  a.rows = p.rows;
+  a.cpb = p.cpb;
+  a.cpr = make_fastdiv(p.cpr ? p.cpr : 1);
+  a.lg = p.gran == G_GROUP ? log2_exact(p.group / 16) : 0;
+  if (p.fmt == F_NVFP4) a.lg = 0;
+  a.ir = IntRange{p.qmin, p.qmax};
+  switch (p.fmt) {
+    case F_INT8: fwd_codes<F_INT8>(p, a, st); break;
+    case F_INT4: fwd_codes<F_INT4>(p, a, st); break;
+    case F_FP8: fwd_codes<F_FP8>(p, a, st); break;
+    default: fwd_codes<F_NVFP4>(p, a, st); break;
+  }
+  return cudaGetLastError();
+}
+
+size_t grad_workspace_bytes(const Problem& p) {
+  if (!grad_needs_partials(p) || p.batch == 0) return 0;
+  return size_t(p.batch) * size_t(grad_parts(p)) * sizeof(double);
+}
+
+cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, const float* scale,
+                              const float* tscale, float* dscale, float* dtscale, void* dx,
+                              int accumulate, double* ws, cudaStream_t st) {
+  const bool partials = grad_needs_partials(p);
+  float* out = (p.fmt == F_NVFP4 && p.mode == 1) ? dtscale : dscale;
+  if (p.batch == 0) return cudaSuccess;
+  if (p.cpb == 0) {
+    // empty rows: every gradient is an empty sum
+    if (!accumulate) {
+      size_t n = partials ? size_t(p.batch)
+                          : (p.gran == G_ROW ? size_t(p.batch * p.rows) : 0);
+      if (n) {
+        cudaError_t e = cudaMemsetAsync(out, 0, n * sizeof(float), st);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    return cudaGetLastError();
+  }
+  GradArgs a;
+  a.x = static_cast<const uint8_t*>(x);
+  a.dy = static_cast<const uint8_t*>(dy);
+  a.dx = static_cast<uint8_t*>(dx);
+  a.scale = scale;
+  a.tscale = tscale;
+  a.dscale = dscale;
+  a.ws = ws;
+  a.batch = p.batch;
+  a.rows = p.rows;
+  a.cpb = p.cpb;
+  a.cpr = make_fastdiv(p.cpr);
+  a.lg = grad_unit_lg(p);
+  a.ir = IntRange{p.qmin, p.qmax};
+  a.accumulate = accumulate;
+  a.nparts = partials ? grad_parts(p) : 0;
+  switch (p.fmt) {
+    case F_INT8: grad_fmt<F_INT8>(p, a, st); break;
+    case F_INT4: grad_fmt<F_INT4>(p, a, st); break;
+    case F_FP8: grad_fmt<F_FP8>(p, a, st); break;
+    default: grad_fmt<F_NVFP4>(p, a, st); break;
+  }
+  if (partials) {
+    int64_t blocks = (p.batch + 7) / 8;
+    if (blocks > 65535) blocks = 65535;
+    reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, a.nparts, p.batch, out, accumulate);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace aqfq

@@ -1,0 +1,201 @@
+"""The five fake-quant workloads as sequences of C-ABI calls on device buffers.
+
+A workload owns its device tensors (seeded synthetic inputs, scales
+initialised on the GPU by aqfq_scale_init, outputs) and lists the calls of one
+step of its hot path with each call's algorithmic bytes:
+
+  grouped_nvfp4  MoE expert stacks gate_up [128,1536,2048] and down
+                 [128,2048,768], Student-t(4)*0.02 with 0.05 % outliers x20:
+                 grouped NVFP4 QDQ forward + per-block scale gradient
+  nvfp4_wa       NVFP4 weight [4096,4096] (learned block scales) and
+                 activations [8192,4096] (dynamic block scales, learned
+                 tensor scale, STE input gradient): forward + scale gradients
+  int4_fp8       INT4 g128 stack [128,1536,2048] and FP8 per-channel dense
+                 [8192,8192]: forward + scale gradients
+  observer_fp8   per-head min/max of [65536,32,128] activations, per-head
+                 scale, per-head E4M3 QDQ
+  int8_channel   INT8 per-channel weight [256,512]: forward + scale gradient
+
+Algorithmic bytes count what the call must move once: inputs read, outputs
+written (no codes: the steps do not request them).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Callable
+
+import torch
+
+from . import aqfq, synth
+
+Q = aqfq.qspec
+
+
+@dataclass
+class Op:
+    name: str
+    kernel: str
+    elems: int
+    bytes: int
+    run: Callable[[torch.cuda.Stream], None]
+    launches: int = 1  # kernels the call launches
+
+
+@dataclass
+class Workload:
+    name: str
+    description: str
+    config: dict
+    ops: list = field(default_factory=list)
+    inputs: dict = field(default_factory=dict)    # name -> device tensor a user uploads
+    outputs: dict = field(default_factory=dict)   # name -> device tensor a user reads back
+
+    @property
+    def bytes_per_step(self) -> int:
+        return sum(o.bytes for o in self.ops)
+
+    @property
+    def elems_per_step(self) -> int:
+        return sum(o.elems for o in self.ops)
+
+    def step(self, stream):
+        for o in self.ops:
+            o.run(stream)
+
+
+def _nvfp4_stack(name, w, dy, dev, ops, inputs, outputs, grouped=True):
+    E, N, K = w.shape
+    sp = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16)
+    s = torch.empty(E * N * K // 16, device=dev)
+    g = torch.empty(E, device=dev)
+    aqfq.aqfq_scale_init(sp, w, s, g)
+    y = torch.empty_like(w)
+    ds = torch.empty_like(s)
+    n = w.numel()
+    fwd = aqfq.aqfq_grouped_qdq if grouped else aqfq.aqfq_qdq_fwd
+    ops.append(Op(f"qdq_fwd {name}", "nvfp4_fwd", n, n * 2 + n // 16 * 4 + n * 2,
+                  lambda st: fwd(sp, w, s, g, y, stream=st)))
+    ops.append(Op(f"scale_grad {name}", "nvfp4_grad", n, n * 4 + n // 16 * 8,
+                  lambda st: aqfq.aqfq_scale_grad(sp, w, dy, s, g, dscale=ds, stream=st)))
+    inputs.update({f"{name}": w, f"dy_{name}": dy, f"scale_{name}": s, f"tscale_{name}": g})
+    outputs.update({f"y_{name}": y, f"dscale_{name}": ds})
+    return sp, s, g
+
+
+def grouped_nvfp4(dev, seed=0, experts=None):
+    d = synth.cfg3(dev, seed, experts)
+    wl = Workload("grouped_nvfp4",
+                  "grouped NVFP4 MoE expert stacks gate_up [E,1536,2048] + down [E,2048,768], "
+                  "vectorised QDQ fwd + per-block scale grad",
+                  {"workload": "grouped_nvfp4_moe_stacks",
+                   "gate_up": list(d["gate_up"].shape), "down": list(d["down"].shape),
+                   "format": "nvfp4 (e2m1, 16-elem blocks, e4m3 block scale, fp32 tensor scale)",
+                   "values": "student-t(4)*0.02, 0.05% outliers x20", "scale_init": "amax/6, amax/2688"})
+    for nm in ("gate_up", "down"):
+        _nvfp4_stack(nm, d[nm], d[f"dy_{nm}"], dev, wl.ops, wl.inputs, wl.outputs)
+    # order: both forwards, then both gradients (forward pass, then backward pass)
+    wl.ops = [wl.ops[0], wl.ops[2], wl.ops[1], wl.ops[3]]
+    return wl
+
+
+def nvfp4_wa(dev, seed=0):
+    d = synth.cfg2(dev, seed)
+    wl = Workload("nvfp4_wa", "NVFP4 weight [4096,4096] + activations [8192,4096]",
+                  {"workload": "nvfp4_weight_activation", "w": [4096, 4096], "a": [8192, 4096]})
+    w = d["w"].unsqueeze(0)
+    _nvfp4_stack("w", w, d["dy_w"].unsqueeze(0), dev, wl.ops, wl.inputs, wl.outputs, grouped=False)
+    a, dya = d["a"].unsqueeze(0), d["dy_a"].unsqueeze(0)
+    spd = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16, mode=aqfq.SCALE_DYNAMIC_BLOCK)
+    ga = torch.empty(1, device=dev)
+    aqfq.aqfq_scale_init(spd, a, None, ga)
+    ya, dxa = torch.empty_like(a), torch.empty_like(a)
+    dga = torch.empty(1, device=dev)
+    ws = torch.empty(max(1, aqfq.aqfq_scale_grad_workspace_bytes(spd, *a.shape) // 8),
+                     dtype=torch.float64, device=dev)
+    n = a.numel()
+    wl.ops.insert(1, Op("qdq_fwd act", "nvfp4_act_fwd", n, 4 * n,
+                        lambda st: aqfq.aqfq_qdq_fwd(spd, a, None, ga, ya, stream=st)))
+    wl.ops.append(Op("scale_grad act (+dx)", "nvfp4_act_grad", n, 6 * n,
+                     lambda st: aqfq.aqfq_scale_grad(spd, a, dya, None, ga, dtensor_scale=dga,
+                                                     dx=dxa, workspace=ws, stream=st), 2))
+    wl.inputs.update({"a": a, "dy_a": dya, "tscale_a": ga})
+    wl.outputs.update({"y_a": ya, "dx_a": dxa, "dtscale_a": dga})
+    return wl
+
+
+def int4_fp8(dev, seed=0):
+    d = synth.cfg4(dev, seed)
+    wl = Workload("int4_fp8", "INT4 g128 stack [128,1536,2048] + FP8 per-channel [8192,8192]",
+                  {"workload": "int4_g128_stack_fp8_channel_dense"})
+    st4 = Q(aqfq.INT4, aqfq.PER_GROUP, group=128, qmin=-8, qmax=7)
+    x4, dy4 = d["stack"], d["dy_stack"]
+    s4 = torch.empty(x4.numel() // 128, device=dev)
+    aqfq.aqfq_scale_init(st4, x4, s4, None)
+    y4, ds4 = torch.empty_like(x4), torch.empty_like(s4)
+    n4 = x4.numel()
+    sp8 = Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL)
+    x8, dy8 = d["dense"].unsqueeze(0), d["dy_dense"].unsqueeze(0)
+    s8 = torch.empty(x8.shape[1], device=dev)
+    aqfq.aqfq_scale_init(sp8, x8, s8, None)
+    y8, ds8 = torch.empty_like(x8), torch.empty_like(s8)
+    n8 = x8.numel()
+    wl.ops = [
+        Op("qdq_fwd int4 stack", "int4_fwd", n4, 4 * n4 + n4 // 128 * 4,
+           lambda st: aqfq.aqfq_grouped_qdq(st4, x4, s4, None, y4, stream=st)),
+        Op("qdq_fwd fp8 dense", "fp8_fwd", n8, 4 * n8,
+           lambda st: aqfq.aqfq_qdq_fwd(sp8, x8, s8, None, y8, stream=st)),
+        Op("scale_grad int4 stack", "int4_grad", n4, 4 * n4 + n4 // 128 * 8,
+           lambda st: aqfq.aqfq_scale_grad(st4, x4, dy4, s4, None, dscale=ds4, stream=st)),
+        Op("scale_grad fp8 dense", "fp8_grad", n8, 4 * n8,
+           lambda st: aqfq.aqfq_scale_grad(sp8, x8, dy8, s8, None, dscale=ds8, stream=st)),
+    ]
+    wl.inputs.update({"stack": x4, "dy_stack": dy4, "scale_stack": s4, "dense": x8,
+                      "dy_dense": dy8, "scale_dense": s8})
+    wl.outputs.update({"y_stack": y4, "dscale_stack": ds4, "y_dense": y8, "dscale_dense": ds8})
+    return wl
+
+
+def observer_fp8(dev, seed=0):
+    d = synth.cfg5(dev, seed)
+    x = d["act"]
+    T, H, D = x.shape
+    wl = Workload("observer_fp8", "per-head observer + E4M3 QDQ on [65536,32,128]",
+                  {"workload": "per_head_observer_fp8", "act": [T, H, D]})
+    mn, mx, s = (torch.empty(H, device=dev) for _ in range(3))
+    y = torch.empty_like(x)
+    sp = Q(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    n = x.numel()
+    wl.ops = [
+        Op("observer_minmax", "observer", n, 2 * n,
+           lambda st: aqfq.aqfq_observer_minmax(x, mn, mx, stream=st), 3),
+        Op("minmax_scale", "minmax_scale", H, 12 * H,
+           lambda st: aqfq.aqfq_minmax_scale(mn, mx, 448.0, s, stream=st)),
+        Op("qdq_fwd per-head fp8", "fp8_head_fwd", n, 4 * n,
+           lambda st: aqfq.aqfq_qdq_fwd(sp, x, s, None, y, stream=st)),
+    ]
+    wl.inputs.update({"act": x})
+    wl.outputs.update({"y": y, "scale": s})
+    return wl
+
+
+def int8_channel(dev, seed=0):
+    d = synth.cfg1(dev, seed)
+    w, dy = d["w"].unsqueeze(0), d["dy"].unsqueeze(0)
+    sp = Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127)
+    s = torch.empty(w.shape[1], device=dev)
+    aqfq.aqfq_scale_init(sp, w, s, None)
+    y, ds = torch.empty_like(w), torch.empty_like(s)
+    n = w.numel()
+    wl = Workload("int8_channel", "INT8 per-channel weight [256,512]",
+                  {"workload": "int8_per_channel_weight", "w": [256, 512]})
+    wl.ops = [Op("qdq_fwd int8", "int8_fwd", n, 4 * n + 4 * w.shape[1],
+                 lambda st: aqfq.aqfq_qdq_fwd(sp, w, s, None, y, stream=st)),
+              Op("scale_grad int8", "int8_grad", n, 4 * n + 8 * w.shape[1],
+                 lambda st: aqfq.aqfq_scale_grad(sp, w, dy, s, None, dscale=ds, stream=st))]
+    wl.inputs.update({"w": w, "dy": dy, "scale": s})
+    wl.outputs.update({"y": y, "dscale": ds})
+    return wl
+
+
+BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
+            "observer_fp8": observer_fp8, "int8_channel": int8_channel}
