@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="grouped_nvfp4")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="grouped_nvfp4 only: truncate the expert axis (small profiling case)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     return ap.parse_args()
@@ -295,7 +297,10 @@ def main():
         dist.barrier()
     aqfq.lib()
 
-    wl = workloads.BUILDERS[args.workload](device)
+    if args.experts is not None and args.workload == "grouped_nvfp4":
+        wl = workloads.grouped_nvfp4(device, experts=args.experts)
+    else:
+        wl = workloads.BUILDERS[args.workload](device)
     stream = torch.cuda.Stream(device)
     small = wl.bytes_per_step < 1.5 * 129e6
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if small else None
