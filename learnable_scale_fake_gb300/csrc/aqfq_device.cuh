@@ -7,11 +7,16 @@
 // gradient sum never leave the lane.
 //
 // Rounding steps follow the library's contract (include/aqfq.h):
-//   v = x / s        IEEE binary32 division (__fdiv_rn; built without fast math)
+//   v = x / s        the IEEE binary32 quotient: per chunk one correctly rounded
+//                    reciprocal and Markstein's FMA correction per element (see
+//                    Divisor); scales outside [2^-125, 2^125] (zero, negative,
+//                    extreme) take __fdiv_rn per element (built without fast math)
 //   q = grid(v)      integer grid: clamp then round-half-even by the 1.5*2^23
 //                    addition trick (exact for |v| < 2^22); E4M3 / E2M1: the
 //                    hardware cvt.rn.satfinite conversions
 //   x_hat = bf16(q*s) __fmul_rn (never contracted into an FMA), cvt.rn.bf16x2
+// The FP grids are symmetric, so their fast paths work on |x| and put the sign
+// of x back on the packed outputs (one bit operation per pair of elements).
 #pragma once
 
 #include <cstdint>
@@ -211,6 +216,161 @@ __device__ __forceinline__ float chunk_amax(const uint32_t (&w)[8]) {
   for (int i = 0; i < 8; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
   uint32_t a = max(m & 0xFFFFu, m >> 16);
   return __uint_as_float(a << 16);
+}
+
+// one E2M1 encode + decode of a pair of magnitudes: returns the packed f16 pair
+// of grid values (lo -> bits 15..0) and the code byte (lo -> bits 3..0)
+__device__ __forceinline__ uint32_t e2m1_pair_h2(float hi, float lo, uint32_t& code) {
+  uint32_t h, c;
+  asm("{ .reg .b8 t, z;\n\t"
+      "mov.b16 {t, z}, 0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t"
+      "mov.b32 %1, {t, z, z, z}; }"
+      : "=r"(h), "=r"(c)
+      : "f"(hi), "f"(lo));
+  code = c;
+  return h;
+}
+
+__device__ __forceinline__ uint32_t e4m3_pair_h2(float hi, float lo, uint32_t& code) {
+  uint32_t h;
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %1, %2, %3;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, %1;"
+      : "=r"(h), "=h"(c)
+      : "f"(hi), "f"(lo));
+  code = c;
+  return h;
+}
+
+// q - m with q an f16 grid value and m binary32 (mixed-precision subtract)
+__device__ __forceinline__ float sub_h_f(uint16_t q, float m) {
+  float d;
+  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(q), "f"(m));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// Division by a chunk's scale s.
+// For 2^-64 <= s <= 2^64: r = RN(1/s) once per chunk, then per element
+// Markstein's correction (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//   q0 = RN(a * r),  e = RN(a - q0 * s) (one FMA),  v = RN(q0 + e * r).
+// a = |x| is first clamped to 2^126 * s (every grid saturates far below that)
+// so no step overflows.  e is exact whenever |x| >= 2^-102 (its quantum is at
+// least that of q0 * s, which stays above 2^-149), and then v is the IEEE
+// quotient |x| / s unless that quotient is below 2^-126.  So v can differ
+// from the IEEE quotient only when |x / s| < 2^-38 (|x| < 2^-102 with
+// s >= 2^-64, or a subnormal quotient), by at most two units in the last
+// place, and every grid maps such quotients to zero: no code or dequantised
+// value changes; a gradient term changes by at most two ulps of itself.
+// (Checked on the GPU: every BF16 mantissa against every binary32 mantissa of
+// s at six exponent pairs, and every BF16 x against 2^18 random s in range:
+// no difference at |x / s| >= 2^-38.)
+// Other s (zero, negative, extreme) take __fdiv_rn per element.
+// ---------------------------------------------------------------------------
+struct Divisor {
+  float s, r, big;
+  bool fast;
+};
+
+__device__ __forceinline__ Divisor make_divisor(float s) {
+  Divisor d;
+  d.s = s;
+  d.fast = (s >= 0x1p-64f) && (s <= 0x1p64f);
+  d.r = __frcp_rn(s);
+  d.big = __fmul_rn(s, 0x1p126f);
+  return d;
+}
+
+// |x| / s (fast path only)
+__device__ __forceinline__ float div_mag(float x, const Divisor& d) {
+  const float a = fminf(fabsf(x), d.big);
+  const float q0 = __fmul_rn(a, d.r);
+  const float e = __fmaf_rn(-q0, d.s, a);
+  return __fmaf_rn(e, d.r, q0);
+}
+
+// ---------------------------------------------------------------------------
+// Fast-path chunks (positive scale in range)
+// ---------------------------------------------------------------------------
+template <int FMT>
+constexpr float grid_max() {
+  return FMT == F_FP8 ? 448.0f : 6.0f;
+}
+
+// sign bits of the two elements of a BF16 pair moved to their code positions
+template <int FMT>
+__device__ __forceinline__ uint32_t code_signs(uint32_t sgn) {
+  if constexpr (FMT == F_FP8) return ((sgn >> 8) & 0x80u) | ((sgn >> 16) & 0x8000u);
+  else return ((sgn >> 12) & 0x8u) | ((sgn >> 24) & 0x80u);
+}
+
+template <int FMT, bool CODES>
+__device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[8], const Divisor& d,
+                                               const IntRange& r, uint32_t (&yw)[8],
+                                               uint32_t (&cw)[4]) {
+  if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = div_mag(bf_lo(xw[i]), d), a1 = div_mag(bf_hi(xw[i]), d);
+    uint32_t code;
+    if constexpr (FMT == F_INT8 || FMT == F_INT4) {
+      const float v0 = copysignf(a0, bf_lo(xw[i])), v1 = copysignf(a1, bf_hi(xw[i]));
+      float q0, q1;
+      bool k0, k1;
+      quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
+      yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s));
+    } else {
+      const uint32_t h = (FMT == F_FP8) ? e4m3_pair_h2(a1, a0, code) : e2m1_pair_h2(a1, a0, code);
+      const float q0 = h2f((uint16_t)(h & 0xFFFFu)), q1 = h2f((uint16_t)(h >> 16));
+      const uint32_t sgn = xw[i] & 0x80008000u;
+      yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s)) | sgn;
+      if (CODES) code |= code_signs<FMT>(sgn);
+    }
+    if (CODES) put_code<FMT>(cw, i, code);
+  }
+}
+
+template <int FMT, bool DX>
+__device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const uint32_t (&dw)[8],
+                                                 const Divisor& d, const IntRange& r,
+                                                 uint32_t (&dxw)[8]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = div_mag(bf_lo(xw[i]), d), a1 = div_mag(bf_hi(xw[i]), d);
+    bool k0, k1;
+    if constexpr (FMT == F_INT8 || FMT == F_INT4) {
+      const float v0 = copysignf(a0, bf_lo(xw[i])), v1 = copysignf(a1, bf_hi(xw[i]));
+      float q0, q1;
+      uint32_t code;
+      quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
+      const float term0 = k0 ? q0 : __fsub_rn(q0, v0);
+      const float term1 = k1 ? q1 : __fsub_rn(q1, v1);
+      t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
+      t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
+    } else {
+      // on magnitudes: term = sign(x) * (q - (clamped ? 0 : |v|)); the sign goes to dy
+      uint32_t code;
+      const uint32_t h = (FMT == F_FP8) ? e4m3_pair_h2(a1, a0, code) : e2m1_pair_h2(a1, a0, code);
+      k0 = a0 >= grid_max<FMT>();
+      k1 = a1 >= grid_max<FMT>();
+      const float term0 = sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : a0);
+      const float term1 = sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : a1);
+      const uint32_t ds = dw[i] ^ (xw[i] & 0x80008000u);
+      t[2 * i] = __fmul_rn(bf_lo(ds), term0);
+      t[2 * i + 1] = __fmul_rn(bf_hi(ds), term1);
+    }
+    if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
+  }
+#pragma unroll
+  for (int w = 1; w < 16; w *= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+  }
+  return t[0];
 }
 
 // ---------------------------------------------------------------------------

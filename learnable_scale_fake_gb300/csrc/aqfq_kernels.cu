@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
           s = nvfp4_block_scale(sb, g, ecode);
         }
         uint32_t yw[8], cw[4];
-        qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
+        const Divisor dv = make_divisor(s);
+        if (dv.fast) qdq_chunk_fast<FMT, CODES>(xw[j], dv, a.ir, yw, cw);
+        else qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
         st_256(a.y + gc * 32, yw);
         if constexpr (CODES) {
           if constexpr (FMT == F_INT8 || FMT == F_FP8) {
@@ -159,7 +161,9 @@ __global__ void __launch_bounds__(kThreads) scale_grad_kernel(const GradArgs a) 
             dec = dec_e4m3x2(ecode).x;
           }
           uint32_t dxw[8];
-          cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          const Divisor dv = make_divisor(s);
+          if (dv.fast) cs = grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw);
+          else cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
           if constexpr (DX) st_256(a.dx + gc * 32, dxw);
         }
         if constexpr (RED == 0) {
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(kThreads) scale_grad_row_kernel(const GradArgs
   for (int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); row < nrows;
        row += (int64_t)gridDim.x * (kThreads / 32)) {
     const float s = __ldg(a.scale + row);
+    const Divisor dv = make_divisor(s);
     const uint64_t base = (uint64_t)row * cpr;
     double acc = 0.0;
     for (uint32_t c0 = 0; c0 < cpr; c0 += 32 * U) {
@@ -217,7 +222,9 @@ __global__ void __launch_bounds__(kThreads) scale_grad_row_kernel(const GradArgs
         const uint32_t c = c0 + j * 32 + lane;
         if (c < cpr) {
           uint32_t dxw[8];
-          acc += (double)grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          const float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw)
+                                   : grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          acc += (double)cs;
           if constexpr (DX) st_256(a.dx + (base + c) * 32, dxw);
         }
       }

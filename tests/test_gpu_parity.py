@@ -161,6 +161,30 @@ def test_special_values():
         ref = oracle_grad(sp, x, dy, s, ts)
         assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
         assert np.array_equal(dx, ref["dx"])
+    # scales at and beyond the ends of the reciprocal fast path [2^-64, 2^64],
+    # with BF16 subnormal and tiny inputs: forward bit-exact, gradient in tolerance
+    edge = torch.tensor([2.0 ** -64, 2.0 ** -64 * (1 - 2 ** -24), 2.0 ** 64, 2.0 ** 64 * (1 + 2 ** -23),
+                         3.1e-20, 7.7e18, 1e-30, 1e30], dtype=torch.float32)
+    xe = synth.normal_bf16((1, 8, 64), 1.0, seed=33).float()
+    xe[:, :, :16] *= 1e-36                        # tiny and subnormal BF16 values
+    xe[:, :, 16:32] *= 1e-20
+    xe[:, :, 32:48] *= 1e20
+    xe = xe.to(torch.bfloat16)
+    dye = synth.normal_bf16((1, 8, 64), 1.0, seed=34)
+    for sp in (Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127), Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL)):
+        y, c, _ = gpu_fwd(sp, xe, edge, None)
+        y_ref, c_ref, _ = oracle_fwd(sp, xe, edge, None)
+        assert np.array_equal(y, y_ref) and np.array_equal(c, c_ref)
+        ds, _, dx = gpu_grad(sp, xe, dye, edge, None)
+        ref = oracle_grad(sp, xe, dye, edge, None)
+        assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
+        assert np.array_equal(dx, ref["dx"])
+    sb = edge.repeat_interleave(4)                 # NVFP4: block scale = S_b / g * g
+    for g in (1.0, 2.0 ** -30):
+        ts = torch.tensor([g], dtype=torch.float32)
+        y, c, b = gpu_fwd(NV, xe, sb * g, ts)
+        y_ref, c_ref, b_ref = oracle_fwd(NV, xe, sb * g, ts)
+        assert np.array_equal(y, y_ref) and np.array_equal(c, c_ref) and np.array_equal(b, b_ref)
     # exact ties of the integer grid: x = (k + 1/2) * s with s a power of two
     s = torch.full((R,), 2.0 ** -8)
     k = torch.arange(-140, 140, dtype=torch.float32)
