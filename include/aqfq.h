@@ -159,6 +159,28 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
                             void* dx, int accumulate, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* aqfq_scale_grad for callers that cannot allocate device memory (no
+ * counterpart in the pages: a library convenience).  Some callers cannot hand
+ * over a scratch buffer: a plugin inside a framework that owns all device
+ * memory through its own pool and gives the plugin no allocation hook, or a
+ * latency-critical path where a cudaMalloc, which may synchronise the device,
+ * is not acceptable.  This call takes the scratch of the per-tensor and
+ * NVFP4 tensor-scale reductions from a 128 KiB array inside the library (held
+ * by every GPU that loads the library until the process exits) and allocates
+ * nothing.  Arguments and results as aqfq_scale_grad without the workspace.
+ *   - Returns AQFQ_ERR_WORKSPACE when aqfq_scale_grad_workspace_bytes(...)
+ *     exceeds 128 KiB (16384 partial sums).
+ *   - All calls share the array: calls whose kernels may overlap on the GPU
+ *     (unordered streams) race.  Nothing needs clearing between calls.
+ *   - The first call on a device looks the array's device address up (device
+ *     current at the call) and caches it; make that first call before any
+ *     stream capture. */
+aqfq_status aqfq_scale_grad_noalloc(const aqfq_qspec* spec, const void* x, const void* dy,
+                                    int64_t batch, int64_t rows, int64_t K, const float* scale,
+                                    const float* tensor_scale, float* dscale,
+                                    float* dtensor_scale, void* dx, int accumulate,
+                                    void* stream);
+
 /* Bytes of device scratch aqfq_scale_grad needs for these arguments (0 when
  * none); returns 0 for arguments aqfq_scale_grad would reject. */
 size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, int64_t rows,

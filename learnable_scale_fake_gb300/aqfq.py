@@ -27,7 +27,7 @@ STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_AL
           4: "AQFQ_ERR_UNSUPPORTED", 5: "AQFQ_ERR_WORKSPACE", 6: "AQFQ_ERR_CUDA"}
 
 # every symbol include/aqfq.h declares
-EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_scale_grad",
+EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_scale_grad", "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
            "aqfq_scale_init", "aqfq_status_string", "aqfq_version")
 
@@ -64,6 +64,7 @@ def lib():
                 "aqfq_qdq_fwd": (i32, [S, P, i64, i64, i64, P, P, P, P, P, P]),
                 "aqfq_grouped_qdq": (i32, [S, P, i64, i64, i64, P, P, P, P, P, P]),
                 "aqfq_scale_grad": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P, sz, P]),
+                "aqfq_scale_grad_noalloc": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P]),
                 "aqfq_scale_grad_workspace_bytes": (sz, [S, i64, i64, i64]),
                 "aqfq_observer_minmax": (i32, [P, i64, i64, i64, P, P, i32, P]),
                 "aqfq_minmax_scale": (i32, [P, P, i64, ctypes.c_float, P, P]),
@@ -160,6 +161,20 @@ def aqfq_scale_grad(spec, x, dy, scale, tensor_scale, dscale=None, dtensor_scale
                                _ptr(tensor_scale), _ptr(dscale), _ptr(dtensor_scale), _ptr(dx),
                                int(bool(accumulate)), _ptr(workspace), wsb, _stream(stream))
     _check("aqfq_scale_grad", st)
+
+
+def aqfq_scale_grad_noalloc(spec, x, dy, scale, tensor_scale, dscale=None, dtensor_scale=None,
+                            dx=None, accumulate=False, stream=None):
+    """aqfq_scale_grad without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in 128 KiB scratch is used."""
+    _bf16(x, "x"), _bf16(dy, "dy"), _bf16(dx, "dx")
+    _f32(scale, "scale"), _f32(tensor_scale, "tensor_scale")
+    _f32(dscale, "dscale"), _f32(dtensor_scale, "dtensor_scale")
+    B, R, K = _brk(x)
+    st = lib().aqfq_scale_grad_noalloc(ctypes.byref(spec), _ptr(x), _ptr(dy), B, R, K, _ptr(scale),
+                                       _ptr(tensor_scale), _ptr(dscale), _ptr(dtensor_scale),
+                                       _ptr(dx), int(bool(accumulate)), _stream(stream))
+    _check("aqfq_scale_grad_noalloc", st)
 
 
 def aqfq_observer_minmax(x, min_out, max_out, accumulate=False, stream=None):
