@@ -218,9 +218,20 @@ __device__ __forceinline__ float chunk_amax(const uint32_t (&w)[8]) {
   return __uint_as_float(a << 16);
 }
 
-// one E2M1 encode + decode of a pair of magnitudes: returns the packed f16 pair
-// of grid values (lo -> bits 15..0) and the code byte (lo -> bits 3..0)
-__device__ __forceinline__ uint32_t e2m1_pair_h2(float hi, float lo, uint32_t& code) {
+// E2M1 / E4M3 rounding of a pair followed by the exact decode: returns the
+// packed f16 pair of grid values (element lo -> bits 15..0); the *c forms also
+// return the codes (E2M1: byte, lo in bits 3..0; E4M3: 16 bits, lo in 7..0)
+__device__ __forceinline__ uint32_t e2m1_q2(float hi, float lo) {
+  uint32_t h;
+  asm("{ .reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t; }"
+      : "=r"(h)
+      : "f"(hi), "f"(lo));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t e2m1_q2c(float hi, float lo, uint32_t& code) {
   uint32_t h, c;
   asm("{ .reg .b8 t, z;\n\t"
       "mov.b16 {t, z}, 0;\n\t"
@@ -233,7 +244,17 @@ __device__ __forceinline__ uint32_t e2m1_pair_h2(float hi, float lo, uint32_t& c
   return h;
 }
 
-__device__ __forceinline__ uint32_t e4m3_pair_h2(float hi, float lo, uint32_t& code) {
+__device__ __forceinline__ uint32_t e4m3_q2(float hi, float lo) {
+  uint32_t h;
+  asm("{ .reg .b16 t;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, t; }"
+      : "=r"(h)
+      : "f"(hi), "f"(lo));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t e4m3_q2c(float hi, float lo, uint32_t& code) {
   uint32_t h;
   uint16_t c;
   asm("cvt.rn.satfinite.e4m3x2.f32 %1, %2, %3;\n\t"
@@ -242,6 +263,18 @@ __device__ __forceinline__ uint32_t e4m3_pair_h2(float hi, float lo, uint32_t& c
       : "f"(hi), "f"(lo));
   code = c;
   return h;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t fp_q2(float hi, float lo) {
+  if constexpr (FMT == F_FP8) return e4m3_q2(hi, lo);
+  else return e2m1_q2(hi, lo);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t fp_q2c(float hi, float lo, uint32_t& code) {
+  if constexpr (FMT == F_FP8) return e4m3_q2c(hi, lo, code);
+  else return e2m1_q2c(hi, lo, code);
 }
 
 // q - m with q an f16 grid value and m binary32 (mixed-precision subtract)
@@ -253,47 +286,56 @@ __device__ __forceinline__ float sub_h_f(uint16_t q, float m) {
 
 // ---------------------------------------------------------------------------
 // Division by a chunk's scale s.
-// For 2^-64 <= s <= 2^64: r = RN(1/s) once per chunk, then per element
-// Markstein's correction (P. Markstein, "Computation of elementary functions
-// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
-//   q0 = RN(a * r),  e = RN(a - q0 * s) (one FMA),  v = RN(q0 + e * r).
-// a = |x| is first clamped to 2^126 * s (every grid saturates far below that)
-// so no step overflows.  e is exact whenever |x| >= 2^-102 (its quantum is at
+// When 2^-64 <= s <= 2^64 and the chunk's largest |x| / s stays below 2^100:
+// r = RN(1/s) once per chunk, then per element Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//   q0 = RN(x * r),  e = RN(x - q0 * s) (one FMA),  v = RN(q0 + e * r).
+// No step can overflow.  e is exact whenever |x| >= 2^-102 (its quantum is at
 // least that of q0 * s, which stays above 2^-149), and then v is the IEEE
-// quotient |x| / s unless that quotient is below 2^-126.  So v can differ
-// from the IEEE quotient only when |x / s| < 2^-38 (|x| < 2^-102 with
-// s >= 2^-64, or a subnormal quotient), by at most two units in the last
-// place, and every grid maps such quotients to zero: no code or dequantised
-// value changes; a gradient term changes by at most two ulps of itself.
-// (Checked on the GPU: every BF16 mantissa against every binary32 mantissa of
-// s at six exponent pairs, and every BF16 x against 2^18 random s in range:
-// no difference at |x / s| >= 2^-38.)
-// Other s (zero, negative, extreme) take __fdiv_rn per element.
+// quotient x / s unless that quotient is below 2^-126.  So v can differ from
+// the IEEE quotient only when |x / s| < 2^-38 (|x| < 2^-102 with s >= 2^-64,
+// or a subnormal quotient), by at most two units in the last place, and every
+// grid maps such quotients to zero: no code or dequantised value changes; a
+// gradient term changes by at most two ulps of itself.  (Checked on the GPU
+// against __fdiv_rn: every BF16 mantissa against every binary32 mantissa of s
+// at six exponent pairs, and every BF16 x against 2^18 random s in range:
+// no difference at |x / s| >= 2^-38.)  With x = -0 the steps give +0; the
+// forward therefore divides |x| and puts the sign back itself.
+// The forward checks the chunk's largest |x| before taking the fast path.
+// The gradient does not: a quotient beyond binary32 range makes q0 infinite
+// and v NaN, the NaN reaches the chunk's gradient sum, and the chunk is then
+// recomputed with IEEE division; finite inputs give no NaN otherwise.
+// Chunks outside these bounds take __fdiv_rn per element.
 // ---------------------------------------------------------------------------
 struct Divisor {
-  float s, r, big;
+  float s, r;
   bool fast;
 };
 
 __device__ __forceinline__ Divisor make_divisor(float s) {
   Divisor d;
   d.s = s;
-  d.fast = (s >= 0x1p-64f) && (s <= 0x1p64f);
   d.r = __frcp_rn(s);
-  d.big = __fmul_rn(s, 0x1p126f);
+  d.fast = (s >= 0x1p-64f) && (s <= 0x1p64f);
   return d;
 }
 
-// |x| / s (fast path only)
-__device__ __forceinline__ float div_mag(float x, const Divisor& d) {
-  const float a = fminf(fabsf(x), d.big);
-  const float q0 = __fmul_rn(a, d.r);
-  const float e = __fmaf_rn(-q0, d.s, a);
+// forward: also require the chunk's largest |x| (exact) / s <= 2^100
+__device__ __forceinline__ Divisor make_divisor(float s, float amax) {
+  Divisor d = make_divisor(s);
+  d.fast = d.fast && (__fmul_rn(amax, d.r) <= 0x1p100f);
+  return d;
+}
+
+__device__ __forceinline__ float mdiv(float x, const Divisor& d) {
+  const float q0 = __fmul_rn(x, d.r);
+  const float e = __fmaf_rn(-q0, d.s, x);
   return __fmaf_rn(e, d.r, q0);
 }
 
 // ---------------------------------------------------------------------------
-// Fast-path chunks (positive scale in range)
+// Fast-path chunks (Divisor::fast)
 // ---------------------------------------------------------------------------
 template <int FMT>
 constexpr float grid_max() {
@@ -314,16 +356,18 @@ __device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[8], const Di
   if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float a0 = div_mag(bf_lo(xw[i]), d), a1 = div_mag(bf_hi(xw[i]), d);
-    uint32_t code;
+    uint32_t code = 0;
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
-      const float v0 = copysignf(a0, bf_lo(xw[i])), v1 = copysignf(a1, bf_hi(xw[i]));
+      // the integer grid maps +-0 alike (an integer code has no sign)
+      const float v0 = mdiv(bf_lo(xw[i]), d), v1 = mdiv(bf_hi(xw[i]), d);
       float q0, q1;
       bool k0, k1;
       quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
       yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s));
     } else {
-      const uint32_t h = (FMT == F_FP8) ? e4m3_pair_h2(a1, a0, code) : e2m1_pair_h2(a1, a0, code);
+      // symmetric grid: round |v|, then give x's sign to the value and the code
+      const float a0 = mdiv(fabsf(bf_lo(xw[i])), d), a1 = mdiv(fabsf(bf_hi(xw[i])), d);
+      const uint32_t h = CODES ? fp_q2c<FMT>(a1, a0, code) : fp_q2<FMT>(a1, a0);
       const float q0 = h2f((uint16_t)(h & 0xFFFFu)), q1 = h2f((uint16_t)(h >> 16));
       const uint32_t sgn = xw[i] & 0x80008000u;
       yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s)) | sgn;
@@ -340,29 +384,25 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const 
   float t[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float a0 = div_mag(bf_lo(xw[i]), d), a1 = div_mag(bf_hi(xw[i]), d);
+    // the sign of a zero quotient does not change a gradient term
+    const float v0 = mdiv(bf_lo(xw[i]), d), v1 = mdiv(bf_hi(xw[i]), d);
     bool k0, k1;
+    float term0, term1;
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
-      const float v0 = copysignf(a0, bf_lo(xw[i])), v1 = copysignf(a1, bf_hi(xw[i]));
       float q0, q1;
       uint32_t code;
       quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
-      const float term0 = k0 ? q0 : __fsub_rn(q0, v0);
-      const float term1 = k1 ? q1 : __fsub_rn(q1, v1);
-      t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
-      t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
+      term0 = k0 ? q0 : __fsub_rn(q0, v0);
+      term1 = k1 ? q1 : __fsub_rn(q1, v1);
     } else {
-      // on magnitudes: term = sign(x) * (q - (clamped ? 0 : |v|)); the sign goes to dy
-      uint32_t code;
-      const uint32_t h = (FMT == F_FP8) ? e4m3_pair_h2(a1, a0, code) : e2m1_pair_h2(a1, a0, code);
-      k0 = a0 >= grid_max<FMT>();
-      k1 = a1 >= grid_max<FMT>();
-      const float term0 = sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : a0);
-      const float term1 = sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : a1);
-      const uint32_t ds = dw[i] ^ (xw[i] & 0x80008000u);
-      t[2 * i] = __fmul_rn(bf_lo(ds), term0);
-      t[2 * i + 1] = __fmul_rn(bf_hi(ds), term1);
+      const uint32_t h = fp_q2<FMT>(v1, v0);
+      k0 = fabsf(v0) >= grid_max<FMT>();
+      k1 = fabsf(v1) >= grid_max<FMT>();
+      term0 = sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : v0);
+      term1 = sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : v1);
     }
+    t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
+    t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
 #pragma unroll
@@ -374,7 +414,8 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const 
 }
 
 // ---------------------------------------------------------------------------
-// One chunk, forward: y = bf16(q * s), packed codes
+// One chunk, forward, IEEE division per element (any scale; only chunks
+// outside the fast path's bounds come here): y = bf16(q * s)
 // ---------------------------------------------------------------------------
 template <int FMT, bool CODES>
 __device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[8], float s, const IntRange& r,
@@ -396,7 +437,8 @@ __device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[8], float s, cons
 }
 
 // ---------------------------------------------------------------------------
-// One chunk, backward: returns sum_i dy_i * (clamped ? q_i : q_i - v_i), summed
+// One chunk, backward, IEEE division per element (as above):
+// returns sum_i dy_i * (clamped ? q_i : q_i - v_i), summed
 // pairwise in a fixed tree; optional STE mask of dy.  The term q - v is exact
 // in binary32 (q and v are within a factor of two, Sterbenz), so the only
 // roundings are one per product and four levels of the tree.

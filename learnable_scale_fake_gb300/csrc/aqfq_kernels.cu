@@ -24,6 +24,31 @@ namespace aqfq {
 
 namespace {
 
+// Chunks per lane per iteration (U) and minimum resident CTAs per SM asked of
+// the register allocator (MINB), per kernel instantiation, from GB300 sweeps
+// on the five workloads: more resident warps beat deeper per-lane unrolling
+// for the gradient until the register cap starts to spill, which the heavier
+// instantiations (STE input gradient, dynamic block scale, partial sums) do.
+template <int FMT, bool DYN, bool DX, int RED>
+struct GradTune {
+  static constexpr bool heavy = DX || DYN || RED != 0;
+  static constexpr int U = heavy ? 1 : (FMT == F_NVFP4 ? 2 : 3);
+  static constexpr int MINB = heavy ? 1 : (FMT == F_NVFP4 ? 5 : 4);
+};
+template <bool DX>
+struct RowTune {
+  static constexpr int U = 2;
+  static constexpr int MINB = DX ? 1 : 4;
+};
+constexpr int kFwdU = 2;
+
+}  // namespace
+}  // namespace aqfq
+
+namespace aqfq {
+
+namespace {
+
 constexpr int kMaxParts = 1024;  // CTAs per batch entry for the cross-CTA reductions
 
 struct FwdArgs {
@@ -76,12 +101,13 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
         const uint64_t gc = base + c;
         float s = sraw[j];
         uint32_t ecode = 0;
+        const float amax = chunk_amax(xw[j]);
         if constexpr (FMT == F_NVFP4) {
-          const float sb = DYN ? __fdiv_rn(chunk_amax(xw[j]), 6.0f) : sraw[j];
+          const float sb = DYN ? __fdiv_rn(amax, 6.0f) : sraw[j];
           s = nvfp4_block_scale(sb, g, ecode);
         }
         uint32_t yw[8], cw[4];
-        const Divisor dv = make_divisor(s);
+        const Divisor dv = make_divisor(s, amax);
         if (dv.fast) qdq_chunk_fast<FMT, CODES>(xw[j], dv, a.ir, yw, cw);
         else qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
         st_256(a.y + gc * 32, yw);
@@ -122,7 +148,8 @@ __device__ __forceinline__ void store_grad(float* p, float g, int accumulate) {
 // RED = 0: one scale per aligned run of (1 << lg) lanes, written directly.
 // RED = 1: one scale (or NVFP4 tensor scale) per batch entry, CTA partials.
 template <int FMT, int GRAN, bool DYN, bool DX, int RED, int U>
-__global__ void __launch_bounds__(kThreads) scale_grad_kernel(const GradArgs a) {
+__global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
+    scale_grad_kernel(const GradArgs a) {
   const int lane = threadIdx.x & 31;
   for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
     const uint64_t base = (uint64_t)b * a.cpb;
@@ -162,8 +189,12 @@ __global__ void __launch_bounds__(kThreads) scale_grad_kernel(const GradArgs a) 
           }
           uint32_t dxw[8];
           const Divisor dv = make_divisor(s);
-          if (dv.fast) cs = grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw);
-          else cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          bool slow = !dv.fast;
+          if (dv.fast) {
+            cs = grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw);
+            slow = isnan(cs);  // a quotient overflowed: redo the chunk exactly
+          }
+          if (slow) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
           if constexpr (DX) st_256(a.dx + gc * 32, dxw);
         }
         if constexpr (RED == 0) {
@@ -197,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) scale_grad_kernel(const GradArgs a) 
 // per-channel gradient for rows whose K is not a power of two <= 512: one warp
 // per row, lanes stride over the row's chunks
 template <int FMT, bool DX, int U>
-__global__ void __launch_bounds__(kThreads) scale_grad_row_kernel(const GradArgs a) {
+__global__ void __launch_bounds__(kThreads, (RowTune<DX>::MINB)) scale_grad_row_kernel(const GradArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t nrows = a.batch * a.rows;
   const uint32_t cpr = a.cpr.d;
@@ -222,8 +253,8 @@ __global__ void __launch_bounds__(kThreads) scale_grad_row_kernel(const GradArgs
         const uint32_t c = c0 + j * 32 + lane;
         if (c < cpr) {
           uint32_t dxw[8];
-          const float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw)
-                                   : grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
+          float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw) : 0.0f;
+          if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
           acc += (double)cs;
           if constexpr (DX) st_256(a.dx + (base + c) * 32, dxw);
         }
@@ -271,8 +302,9 @@ dim3 stream_grid(uint32_t cpb, int64_t batch, int U, int cap) {
 
 template <int FMT, int GRAN, bool DYN, bool CODES>
 void fwd_launch(const FwdArgs& a, cudaStream_t st) {
-  if (a.cpb >= 2u * kThreads) {
-    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 2><<<stream_grid(a.cpb, a.batch, 2, 0), kThreads, 0, st>>>(a);
+  constexpr int U = kFwdU;
+  if (U > 1 && a.cpb >= uint32_t(U) * kThreads) {
+    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, U><<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
   } else {
     qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 1><<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
   }
@@ -299,16 +331,18 @@ void fwd_codes(const Problem& p, const FwdArgs& a, cudaStream_t st) {
   else fwd_gran<FMT, false>(p, a, st);
 }
 
-int grad_unroll(uint32_t cpb) { return cpb >= 2u * kThreads ? 2 : 1; }
+// unroll actually used by a gradient launch (U of the traits, or 1 when the
+// batch entry has fewer than U * 256 chunks)
+int grad_unroll(uint32_t cpb, int U) { return cpb >= uint32_t(U) * kThreads ? U : 1; }
 
 bool grad_needs_partials(const Problem& p) {
   return (p.fmt == F_NVFP4 && p.mode == 1) || (p.fmt != F_NVFP4 && p.gran == G_TENSOR);
 }
 
-int grad_parts(const Problem& p) {
-  const int U = grad_unroll(p.cpb);
-  return (int)stream_grid(p.cpb, 1, U, kMaxParts).x;
-}
+// every partial-sum (RED = 1) instantiation is "heavy": U = 1
+static_assert(GradTune<F_NVFP4, true, false, 1>::U == 1 && GradTune<F_FP8, false, false, 1>::U == 1,
+              "partial-sum kernels are launched with one chunk per lane");
+int grad_parts(const Problem& p) { return (int)stream_grid(p.cpb, 1, 1, kMaxParts).x; }
 
 // block-path lanes per unit (log2), or -1 when the row kernel is needed
 int grad_unit_lg(const Problem& p) {
@@ -323,9 +357,10 @@ int grad_unit_lg(const Problem& p) {
 
 template <int FMT, int GRAN, bool DYN, bool DX, int RED>
 void grad_launch(const GradArgs& a, cudaStream_t st) {
-  if (grad_unroll(a.cpb) == 2) {
-    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 2>
-        <<<stream_grid(a.cpb, a.batch, 2, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
+  constexpr int U = GradTune<FMT, DYN, DX, RED>::U;
+  if (U > 1 && grad_unroll(a.cpb, U) == U) {
+    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U>
+        <<<stream_grid(a.cpb, a.batch, U, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
   } else {
     scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>
         <<<stream_grid(a.cpb, a.batch, 1, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
@@ -347,7 +382,7 @@ void grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
       int64_t blocks = (nrows + kThreads / 32 - 1) / (kThreads / 32);
       if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
       if (blocks < 1) blocks = 1;
-      scale_grad_row_kernel<FMT, DX, 2><<<(unsigned)blocks, kThreads, 0, st>>>(a);
+      scale_grad_row_kernel<FMT, DX, RowTune<DX>::U><<<(unsigned)blocks, kThreads, 0, st>>>(a);
     }
   }
 }
