@@ -73,9 +73,9 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def stored_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary of `kernel`, if the
-    summary was taken on the current sources; else None."""
+def stored_traffic(op_name):
+    """DRAM bytes per launch of op `op_name` from the committed ncu summary, if
+    the summary was taken on the current sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
@@ -83,7 +83,7 @@ def stored_traffic(kernel):
     for line in open(p):
         tok = line.strip().strip("|").split("|")
         tok = [t.strip() for t in tok]
-        if len(tok) >= 3 and tok[0] == kernel and tok[2] == digest:
+        if len(tok) >= 3 and tok[0] == op_name and tok[2] == digest:
             try:
                 return int(tok[1])
             except ValueError:
@@ -354,7 +354,7 @@ def main():
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
             if peak_kind == "measured" else "fallback",
-            "traffic": stored_traffic(dom_op.kernel),
+            "traffic": stored_traffic(dom_op.name),
             "algorithmic_bytes_per_launch": dom_op.bytes}
 
     # ---- end to end through the public API with host buffers ----
