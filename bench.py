@@ -93,7 +93,7 @@ def stored_traffic(op_name):
 
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -113,7 +113,10 @@ class Clocks:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin, t_end):
+        """Samples whose timestamp lies in [t_begin, t_end] (host wall clock,
+        seconds); if the region was shorter than the sampling period, the
+        sample closest to the region's middle."""
         if self.proc is None:
             return None
         time.sleep(0.05)
@@ -124,19 +127,31 @@ class Clocks:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 6]
+        raw = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 7]
         os.unlink(self.file.name)
-        if not rows:
+        rows = []
+        for r in raw:
+            try:
+                ts = time.mktime(time.strptime(r[0].strip()[:19], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0" + r[0].strip()[19:]) if "." in r[0] else 0.0
+                rows.append((ts, [c.strip() for c in r[1:]]))
+            except ValueError:
+                continue
+        inside = [r for t, r in rows if t_begin <= t <= t_end]
+        if not inside and rows:
+            mid = 0.5 * (t_begin + t_end)
+            inside = [min(rows, key=lambda tr: abs(tr[0] - mid))[1]]
+        if not inside:
             return {"samples": 0}
-        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        sm = [float(r[0]) for r in inside if r[0].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" == r[3 + i].strip()})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3 + i] == "Active"})
         try:
-            smax = float(rows[0][1])
+            smax = float(inside[0][1])
         except ValueError:
             smax = None
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(inside)}
 
 
 # ---------------------------------------------------------------------------------------
@@ -321,6 +336,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    wall0 = time.time()
     with torch.cuda.stream(stream):
         t0.record(stream)
         for k in range(args.steps):
@@ -332,7 +348,8 @@ def main():
                 ev[k][i][1].record(stream)
         t1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     if dist is not None:
         dist.barrier()
     per_op = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
@@ -360,39 +377,25 @@ def main():
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                   for k, v in wl.inputs.items()}
-        for k, v in wl.inputs.items():
-            host_in[k].copy_(v)
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                    for k, v in wl.outputs.items()}
+        host_in, host_out = wl.host_buffers()
         bi = sum(v.numel() * v.element_size() for v in host_in.values())
         bo = sum(v.numel() * v.element_size() for v in host_out.values())
-
-        def e2e_step():
-            for k, v in wl.inputs.items():
-                v.copy_(host_in[k], non_blocking=True)
-            wl.step(stream)
-            for k, v in wl.outputs.items():
-                host_out[k].copy_(v, non_blocking=True)
-
+        streams = (torch.cuda.Stream(device), stream, torch.cuda.Stream(device))
         n_e2e = max(3, min(args.steps, 20))
-        with torch.cuda.stream(stream):
-            e2e_step()
+        wl.e2e_step(host_in, host_out, streams)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(n_e2e):
-                e2e_step()
-            e1.record(stream)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            wl.e2e_step(host_in, host_out, streams)
+        e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, device)
         e2e = {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
-               "steps": n_e2e}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 3),
+               "steps": n_e2e, "pipelined_slices": len(getattr(wl, "slices", None) or [])}
 
     # ---- CPU oracle on a bounded sample (rank 0, one GPU) ----
     cpu = None

@@ -62,6 +62,56 @@ class Workload:
         for o in self.ops:
             o.run(stream)
 
+    # ---- end to end with host buffers -------------------------------------------
+    def host_buffers(self):
+        """Pinned host copies of the inputs (filled from the device) and pinned
+        host buffers for the outputs."""
+        hin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in self.inputs.items()}
+        for k, v in self.inputs.items():
+            hin[k].copy_(v)
+        hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in self.outputs.items()}
+        return hin, hout
+
+    def e2e_step(self, hin, hout, streams):
+        """One step from host buffers: upload every input, run the step, download
+        every output.  Workloads with slices pipeline upload / compute /
+        download over them on three streams."""
+        up, comp, down = streams
+        slices = getattr(self, "slices", None)
+        if not slices:
+            with torch.cuda.stream(comp):
+                for k, v in self.inputs.items():
+                    v.copy_(hin[k], non_blocking=True)
+                self.step(comp)
+                for k, v in self.outputs.items():
+                    hout[k].copy_(v, non_blocking=True)
+            return
+        # uploads of this step wait for everything queued on the compute stream
+        # (the previous step, including its downloads)
+        ev_start = torch.cuda.Event()
+        ev_start.record(comp)
+        up.wait_event(ev_start)
+        for sl in slices:
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(up):
+                for name, (dev_t, host_t) in sl.inputs(self, hin).items():
+                    dev_t.copy_(host_t, non_blocking=True)
+                ev_in.record(up)
+            ev_done = torch.cuda.Event()
+            with torch.cuda.stream(comp):
+                comp.wait_event(ev_in)
+                for run in sl.ops:
+                    run(comp)
+                ev_done.record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done)
+                for name, (dev_t, host_t) in sl.outputs(self, hout).items():
+                    host_t.copy_(dev_t, non_blocking=True)
+        # the caller's stream (comp) ends the step after the last download
+        ev_end = torch.cuda.Event()
+        ev_end.record(down)
+        comp.wait_event(ev_end)
+
 
 def _nvfp4_stack(name, w, dy, dev, ops, inputs, outputs, grouped=True):
     E, N, K = w.shape
@@ -82,6 +132,38 @@ def _nvfp4_stack(name, w, dy, dev, ops, inputs, outputs, grouped=True):
     return sp, s, g
 
 
+class _ExpertSlice:
+    """Experts [e0, e1) of the grouped workload: device/host views of that slice
+    of every per-expert tensor and the public calls on them."""
+
+    def __init__(self, wl, e0, e1):
+        self.e0, self.e1 = e0, e1
+        self.ops = []
+        sp = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16)
+        for nm in ("gate_up", "down"):
+            x, dy = wl.inputs[nm][e0:e1], wl.inputs[f"dy_{nm}"][e0:e1]
+            s, g = self._rows(wl.inputs[f"scale_{nm}"], wl), wl.inputs[f"tscale_{nm}"][e0:e1]
+            y, ds = wl.outputs[f"y_{nm}"][e0:e1], self._rows(wl.outputs[f"dscale_{nm}"], wl)
+            self.ops.append(lambda st, x=x, s=s, g=g, y=y: aqfq.aqfq_grouped_qdq(sp, x, s, g, y, stream=st))
+            self.ops.append(lambda st, x=x, dy=dy, s=s, g=g, ds=ds:
+                            aqfq.aqfq_scale_grad(sp, x, dy, s, g, dscale=ds, stream=st))
+
+    def _rows(self, flat, wl):
+        E = wl.inputs["gate_up"].shape[0]
+        return flat.view(E, -1)[self.e0:self.e1].reshape(-1)
+
+    def _pairs(self, dev, host, wl):
+        E = wl.inputs["gate_up"].shape[0]
+        return {k: (v.view(E, -1)[self.e0:self.e1], host[k].view(E, -1)[self.e0:self.e1])
+                for k, v in dev.items()}
+
+    def inputs(self, wl, hin):
+        return self._pairs(wl.inputs, hin, wl)
+
+    def outputs(self, wl, hout):
+        return self._pairs(wl.outputs, hout, wl)
+
+
 def grouped_nvfp4(dev, seed=0, experts=None):
     d = synth.cfg3(dev, seed, experts)
     wl = Workload("grouped_nvfp4",
@@ -95,6 +177,11 @@ def grouped_nvfp4(dev, seed=0, experts=None):
         _nvfp4_stack(nm, d[nm], d[f"dy_{nm}"], dev, wl.ops, wl.inputs, wl.outputs)
     # order: both forwards, then both gradients (forward pass, then backward pass)
     wl.ops = [wl.ops[0], wl.ops[2], wl.ops[1], wl.ops[3]]
+    # end to end: 8 slices of experts, upload / compute / download overlapped
+    E = d["gate_up"].shape[0]
+    n = max(1, min(8, E))
+    bounds = [E * i // n for i in range(n + 1)]
+    wl.slices = [_ExpertSlice(wl, a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
     return wl
 
 
