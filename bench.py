@@ -1,7 +1,8 @@
 """Benchmark of the fake-quant hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload grouped_nvfp4|nvfp4_wa|int4_fp8|observer_fp8|int8_channel]
+                    [--workload grouped_nvfp4|nvfp4_wa|int4_fp8|observer_fp8|int8_channel|
+                                head_fp8_learned]
 
 One step = one pass of the workload's whole hot path: for the default
 workload (grouped NVFP4 MoE expert stacks, gate_up [128,1536,2048] + down
@@ -159,8 +160,9 @@ class Clocks:
 # ---------------------------------------------------------------------------------------
 
 def _oracle_jobs(name, inputs):
-    """(label, x, dy, oracle spec, rows per unit) for the workload's tensors;
-    x / dy are [units, ...] so that a sample is a leading slice."""
+    """(label, x, dy, oracle spec, algorithmic bytes per element of fwd + grad)
+    for the workload's tensors; x / dy are [units, ...] so that a sample is a
+    leading slice.  The bytes per element match the workload's GPU ops."""
     import oracle as O
 
     def flat(t):
@@ -168,23 +170,26 @@ def _oracle_jobs(name, inputs):
 
     if name == "grouped_nvfp4":
         sp = O.spec(O.NVFP4, O.PER_GROUP, group=16)
-        return [(nm, inputs[nm], inputs[f"dy_{nm}"], sp) for nm in ("gate_up", "down")], "experts"
+        return [(nm, inputs[nm], inputs[f"dy_{nm}"], sp, 8.75) for nm in ("gate_up", "down")], "experts"
     if name == "int4_fp8":
         return [("stack", inputs["stack"], inputs["dy_stack"],
-                 O.spec(O.INT4, O.PER_GROUP, group=128, qmin=-8, qmax=7)),
+                 O.spec(O.INT4, O.PER_GROUP, group=128, qmin=-8, qmax=7), 4.03125 + 4.0625),
                 ("dense", flat(inputs["dense"]).reshape(-1, 64, 8192),
                  flat(inputs["dy_dense"]).reshape(-1, 64, 8192),
-                 O.spec(O.FP8_E4M3, O.PER_CHANNEL))], "leading units (expert / 64 rows)"
+                 O.spec(O.FP8_E4M3, O.PER_CHANNEL), 8.0)], "leading units (expert / 64 rows)"
     if name == "nvfp4_wa":
         return [("w", flat(inputs["w"]).reshape(-1, 64, 4096), flat(inputs["dy_w"]).reshape(-1, 64, 4096),
-                 O.spec(O.NVFP4, O.PER_GROUP, group=16)),
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16), 8.75),
                 ("a", flat(inputs["a"]).reshape(-1, 64, 4096), flat(inputs["dy_a"]).reshape(-1, 64, 4096),
-                 O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK))], \
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK), 10.0)], \
             "leading units of 64 rows"
     if name == "int8_channel":
         return [("w", flat(inputs["w"]).reshape(-1, 16, 512), flat(inputs["dy"]).reshape(-1, 16, 512),
-                 O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127))], "leading units of 16 rows"
-    return [("act", inputs["act"], None, None)], "leading tokens"
+                 O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), 8.0)], "leading units of 16 rows"
+    if name == "head_fp8_learned":
+        return [("act", inputs["act"], inputs["dy"], O.spec(O.FP8_E4M3, O.PER_HEAD), 10.0)], \
+            "leading tokens"
+    return [("act", inputs["act"], None, None, 6.0)], "leading tokens"
 
 
 def oracle_run(name, inputs, k):
@@ -197,7 +202,7 @@ def oracle_run(name, inputs, k):
     jobs, _ = _oracle_jobs(name, inputs)
     nbytes = elems = 0
     secs = 0.0
-    for nm, x, dy, sp in jobs:
+    for nm, x, dy, sp, bpe in jobs:
         kk = min(k, x.shape[0])
         xb = synth.bf16_bits(x[:kk])
         if sp is None:  # observer + scale + per-head E4M3 QDQ
@@ -206,7 +211,7 @@ def oracle_run(name, inputs, k):
             sc = O.minmax_scale(lo, hi, 448.0)
             O.qdq_fwd(O.spec(O.FP8_E4M3, O.PER_HEAD), xb, sc)
             secs += time.perf_counter() - t0
-            nbytes += 6 * xb.size
+            nbytes += int(bpe * xb.size)
             elems += 2 * xb.size
             continue
         db = synth.bf16_bits(dy[:kk])
@@ -219,20 +224,21 @@ def oracle_run(name, inputs, k):
         secs += time.perf_counter() - t0
         m = xb.size
         elems += 2 * m
-        nbytes += int(m * (8.75 if (sp.fmt == O.NVFP4 and sp.mode == O.SCALE_LEARNED) else 8.0))
+        nbytes += int(m * bpe)
     return int(nbytes), elems, secs
 
 
-def oracle_pick(name, inputs, budget_s):
-    """Grows the sample (x4) until one oracle pass takes about budget_s / 4."""
+def oracle_pick(name, inputs, target_s):
+    """Grows the sample (x2) until one oracle pass takes at least target_s / 2
+    (so a pass lasts about target_s / 2 .. target_s), or the inputs run out."""
     jobs, unit = _oracle_jobs(name, inputs)
     limit = min(j[1].shape[0] for j in jobs)
     k = 1
     while True:
         res = oracle_run(name, inputs, k)
-        if res[2] > budget_s / 4 or k >= limit:
+        if res[2] >= target_s / 2 or k >= limit:
             return k, res, f"first {k} {unit} of each tensor"
-        k = min(limit, k * 4)
+        k = min(limit, max(k + 1, int(k * min(4.0, 0.75 * target_s / max(res[2], 1e-3)))))
 
 
 def reference_arm(args):
@@ -243,11 +249,15 @@ def reference_arm(args):
     import oracle
     from learnable_scale_fake_gb300 import synth
 
-    gen = {"grouped_nvfp4": lambda: synth.cfg3("cpu", 0, experts=4), "nvfp4_wa": lambda: synth.cfg2("cpu"),
+    gen = {"grouped_nvfp4": lambda: synth.cfg3("cpu", 0, experts=8), "nvfp4_wa": lambda: synth.cfg2("cpu"),
            "int4_fp8": lambda: synth.cfg4("cpu"), "int8_channel": lambda: synth.cfg1("cpu"),
-           "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)}}
+           "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)},
+           "head_fp8_learned": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0),
+                                        "dy": synth.normal_bf16((4096, 32, 128), 1.0, 1)}}
     inputs = gen[args.workload]()
-    k, _, desc = oracle_pick(args.workload, inputs, budget_s=4.0)
+    # the whole run (warm-up + timed steps) takes about a minute of oracle time
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    k, _, desc = oracle_pick(args.workload, inputs, target_s=per_step)
     runs = []
     for i in range(args.warmup + args.steps):
         r = oracle_run(args.workload, inputs, k)
@@ -402,7 +412,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
 
-        k, _, desc = oracle_pick(args.workload, wl.inputs, budget_s=8.0)
+        k, _, desc = oracle_pick(args.workload, wl.inputs, target_s=20.0)
         nbytes, elems, secs = oracle_run(args.workload, wl.inputs, k)
         cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
                "cores": oracle.num_threads(), "kind": "oracle",

@@ -151,8 +151,11 @@ aqfq_status aqfq_grouped_qdq(const aqfq_qspec* spec, const void* w, int64_t E, i
  *   accumulate    0: overwrite dscale / dtensor_scale; else add to them
  *   workspace     device scratch, >= aqfq_scale_grad_workspace_bytes(...)
  *                 bytes (0 bytes for per-channel / per-group / NVFP4 learned;
- *                 the result is deterministic: fixed reduction order)
- * Not implemented: AQFQ_PER_HEAD (AQFQ_ERR_UNSUPPORTED). */
+ *                 per-tensor, per-head and the NVFP4 tensor scale need it; the
+ *                 result is deterministic: fixed reduction order)
+ * Per-head (x [T, H, D], scale [H], learnable per-head activation scale, e.g.
+ * FP8 attention / KV activations; msModelSlim guide, "FA3Quant"): requires
+ * H * D / 16 <= 2^24. */
 aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
                             int64_t rows, int64_t K, const float* scale,
                             const float* tensor_scale, float* dscale, float* dtensor_scale,

@@ -162,7 +162,6 @@ size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, in
                                        int64_t K) {
   Problem p;
   if (make_problem(spec, batch, rows, K, p) != AQFQ_OK) return 0;
-  if (p.gran == AQFQ_PER_HEAD && p.fmt != AQFQ_NVFP4) return 0;
   return aqfq::grad_workspace_bytes(p);
 }
 
@@ -174,7 +173,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
   Problem p;
   aqfq_status s = make_problem(spec, batch, rows, K, p);
   if (s != AQFQ_OK) return s;
-  if (p.fmt != AQFQ_NVFP4 && p.gran == AQFQ_PER_HEAD) return AQFQ_ERR_UNSUPPORTED;
+  if (p.gran == AQFQ_PER_HEAD && p.rows * (p.K / 16) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
   if (elems(p) > 0 && (!x || !dy)) return AQFQ_ERR_NULL;
   if ((s = check_scales(p, scale, tensor_scale)) != AQFQ_OK) return s;
   const bool dyn = p.fmt == AQFQ_NVFP4 && p.mode == AQFQ_SCALE_DYNAMIC_BLOCK;

@@ -49,7 +49,16 @@ namespace aqfq {
 
 namespace {
 
-constexpr int kMaxParts = 1024;  // CTAs per batch entry for the cross-CTA reductions
+constexpr int kMaxCtasPerSm = 2048 / kThreads;  // resident 256-thread CTAs per SM, at most
+
+// resident CTAs per SM of a kernel at 256 threads (at least 1)
+template <typename Kernel>
+int occupancy(Kernel kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+    n = 1;
+  return n;
+}
 
 struct FwdArgs {
   const uint8_t* x;
@@ -281,6 +290,86 @@ __global__ void reduce_partials_kernel(const double* ws, int nparts, int64_t bat
 }
 
 // ---------------------------------------------------------------------------
+// per-head gradient: x [T, H, D], one scale per head shared by all tokens.
+// The threads used are a multiple of the chunks per token (cpt), so thread j
+// always reads column-chunk j % cpt (one head) of successive tokens and sums
+// its chunk gradients in double; ws[j] holds that partial.  A second kernel
+// adds each head's partials in a fixed order.
+// ---------------------------------------------------------------------------
+struct HeadArgs {
+  const uint8_t* x;
+  const uint8_t* dy;
+  uint8_t* dx;
+  const float* scale;
+  double* ws;
+  uint64_t nchunks;  // T * cpt
+  uint32_t cpt;
+  FastDiv cph;       // chunks per head
+  uint64_t used;     // threads with work (multiple of cpt)
+  IntRange ir;
+};
+
+template <int FMT, bool DX>
+__global__ void __launch_bounds__(kThreads) scale_grad_head_kernel(const HeadArgs a) {
+  const uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (j >= a.used) return;
+  const float s = __ldg(a.scale + fdiv((uint32_t)(j % a.cpt), a.cph));
+  const Divisor dv = make_divisor(s);
+  double acc = 0.0;
+  for (uint64_t c0 = j; c0 < a.nchunks; c0 += 2 * a.used) {
+    uint32_t xw[2][8], dw[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint64_t c = c0 + u * a.used;
+      if (c < a.nchunks) {
+        ld_stream(a.x + c * 32, xw[u]);
+        ld_stream(a.dy + c * 32, dw[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint64_t c = c0 + u * a.used;
+      if (c >= a.nchunks) continue;
+      uint32_t dxw[8];
+      float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[u], dw[u], dv, a.ir, dxw) : 0.0f;
+      if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[u], dw[u], s, a.ir, dxw);
+      acc += (double)cs;
+      if constexpr (DX) st_256(a.dx + c * 32, dxw);
+    }
+  }
+  a.ws[j] = acc;
+}
+
+// dscale[h] = sum over r < used / cpt, c < cph of ws[r * cpt + h * cph + c]
+__global__ void reduce_heads_kernel(const double* ws, uint64_t rounds, uint32_t cpt, uint32_t cph,
+                                    int64_t H, float* out, int accumulate) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t h = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); h < H;
+       h += (int64_t)gridDim.x * (blockDim.x / 32)) {
+    double t = 0.0;
+    const uint64_t n = rounds * cph;
+    for (uint64_t i = lane; i < n; i += 32) t += ws[(i / cph) * cpt + h * cph + (i % cph)];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+    if (lane == 0) store_grad(out + h, (float)t, accumulate);
+  }
+}
+
+// threads used by the per-head gradient: one wave of `ctas_per_sm` CTAs per
+// SM, rounded down to a multiple of the chunks per token (at least one token's
+// worth), and no more than the chunks there are
+uint64_t head_threads(const Problem& p, int ctas_per_sm) {
+  const uint64_t cpt = p.cpr * uint64_t(p.rows);
+  const uint64_t nchunks = uint64_t(p.batch) * cpt;
+  if (cpt == 0) return 0;
+  uint64_t want = uint64_t(sm_count()) * ctas_per_sm * kThreads;
+  uint64_t used = want / cpt * cpt;
+  if (used < cpt) used = cpt;
+  if (used > nchunks) used = nchunks;
+  return used;
+}
+
+// ---------------------------------------------------------------------------
 // host-side dispatch
 // ---------------------------------------------------------------------------
 
@@ -342,7 +431,16 @@ bool grad_needs_partials(const Problem& p) {
 // every partial-sum (RED = 1) instantiation is "heavy": U = 1
 static_assert(GradTune<F_NVFP4, true, false, 1>::U == 1 && GradTune<F_FP8, false, false, 1>::U == 1,
               "partial-sum kernels are launched with one chunk per lane");
-int grad_parts(const Problem& p) { return (int)stream_grid(p.cpb, 1, 1, kMaxParts).x; }
+// CTAs per batch entry of a partial-sum launch: one wave over all entries
+// (ctas_per_sm resident CTAs on every SM), at most one per 256 chunks
+int grad_parts(const Problem& p, int ctas_per_sm) {
+  const int64_t entries = p.batch < 65535 ? p.batch : 65535;
+  int64_t parts = int64_t(sm_count()) * ctas_per_sm / (entries > 0 ? entries : 1);
+  const int64_t need = (int64_t(p.cpb) + kThreads - 1) / kThreads;
+  if (parts > need) parts = need;
+  if (parts < 1) parts = 1;
+  return (int)parts;
+}
 
 // block-path lanes per unit (log2), or -1 when the row kernel is needed
 int grad_unit_lg(const Problem& p) {
@@ -355,42 +453,52 @@ int grad_unit_lg(const Problem& p) {
   return 0;
 }
 
+// returns the CTAs per batch entry of a partial-sum launch (0 otherwise)
 template <int FMT, int GRAN, bool DYN, bool DX, int RED>
-void grad_launch(const GradArgs& a, cudaStream_t st) {
+int grad_launch(const Problem& p, GradArgs a, cudaStream_t st) {
   constexpr int U = GradTune<FMT, DYN, DX, RED>::U;
-  if (U > 1 && grad_unroll(a.cpb, U) == U) {
-    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U>
-        <<<stream_grid(a.cpb, a.batch, U, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
+  if constexpr (RED == 1) {
+    auto k = scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>;
+    a.nparts = grad_parts(p, occupancy(k));
+    k<<<stream_grid(a.cpb, a.batch, 1, a.nparts), kThreads, 0, st>>>(a);
+    return a.nparts;
   } else {
-    scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>
-        <<<stream_grid(a.cpb, a.batch, 1, RED ? kMaxParts : 0), kThreads, 0, st>>>(a);
+    if (U > 1 && grad_unroll(a.cpb, U) == U) {
+      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U>
+          <<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
+    } else {
+      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>
+          <<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
+    }
+    return 0;
   }
 }
 
 template <int FMT, bool DX>
-void grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
+int grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
   if constexpr (FMT == F_NVFP4) {
-    if (p.mode == 1) grad_launch<FMT, G_GROUP, true, DX, 1>(a, st);
-    else grad_launch<FMT, G_GROUP, false, DX, 0>(a, st);
+    if (p.mode == 1) return grad_launch<FMT, G_GROUP, true, DX, 1>(p, a, st);
+    return grad_launch<FMT, G_GROUP, false, DX, 0>(p, a, st);
   } else {
     if (p.gran == G_TENSOR) {
-      grad_launch<FMT, G_TENSOR, false, DX, 1>(a, st);
+      return grad_launch<FMT, G_TENSOR, false, DX, 1>(p, a, st);
     } else if (a.lg >= 0) {  // per-group, or per-channel rows of 16..512 (power of two)
-      grad_launch<FMT, G_GROUP, false, DX, 0>(a, st);
+      return grad_launch<FMT, G_GROUP, false, DX, 0>(p, a, st);
     } else {
       const int64_t nrows = p.batch * p.rows;
       int64_t blocks = (nrows + kThreads / 32 - 1) / (kThreads / 32);
       if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
       if (blocks < 1) blocks = 1;
       scale_grad_row_kernel<FMT, DX, RowTune<DX>::U><<<(unsigned)blocks, kThreads, 0, st>>>(a);
+      return 0;
     }
   }
 }
 
 template <int FMT>
-void grad_fmt(const Problem& p, const GradArgs& a, cudaStream_t st) {
-  if (a.dx) grad_dispatch<FMT, true>(p, a, st);
-  else grad_dispatch<FMT, false>(p, a, st);
+int grad_fmt(const Problem& p, const GradArgs& a, cudaStream_t st) {
+  if (a.dx) return grad_dispatch<FMT, true>(p, a, st);
+  return grad_dispatch<FMT, false>(p, a, st);
 }
 
 }  // namespace
@@ -422,14 +530,72 @@ cudaError_t launch_qdq_fwd(const Problem& p, const void* x, const float* scale,
   return cudaGetLastError();
 }
 
+// Upper bounds over every instantiation (resident CTAs per SM <= 8), for the
+// current device: the launches size their grids from the kernel's occupancy.
 size_t grad_workspace_bytes(const Problem& p) {
+  if (p.fmt != F_NVFP4 && p.gran == G_HEAD)
+    return size_t(head_threads(p, kMaxCtasPerSm)) * sizeof(double);
   if (!grad_needs_partials(p) || p.batch == 0) return 0;
-  return size_t(p.batch) * size_t(grad_parts(p)) * sizeof(double);
+  return size_t(p.batch) * size_t(grad_parts(p, kMaxCtasPerSm)) * sizeof(double);
 }
+
+namespace {
+
+// returns the threads used (one wave of the kernel's resident CTAs)
+template <int FMT, bool DX>
+uint64_t head_launch(const Problem& p, HeadArgs a, cudaStream_t st) {
+  auto k = scale_grad_head_kernel<FMT, DX>;
+  a.used = head_threads(p, occupancy(k));
+  const uint64_t blocks = (a.used + kThreads - 1) / kThreads;
+  k<<<(unsigned)blocks, kThreads, 0, st>>>(a);
+  return a.used;
+}
+
+template <int FMT>
+uint64_t head_fmt(const Problem& p, const HeadArgs& a, cudaStream_t st) {
+  if (a.dx) return head_launch<FMT, true>(p, a, st);
+  return head_launch<FMT, false>(p, a, st);
+}
+
+cudaError_t launch_head_grad(const Problem& p, const void* x, const void* dy, const float* scale,
+                             float* dscale, void* dx, int accumulate, double* ws,
+                             cudaStream_t st) {
+  if (p.rows == 0) return cudaSuccess;
+  if (p.batch == 0 || p.cpr == 0) {  // no elements: every head's gradient is an empty sum
+    if (!accumulate) return cudaMemsetAsync(dscale, 0, size_t(p.rows) * sizeof(float), st);
+    return cudaSuccess;
+  }
+  HeadArgs a;
+  a.x = static_cast<const uint8_t*>(x);
+  a.dy = static_cast<const uint8_t*>(dy);
+  a.dx = static_cast<uint8_t*>(dx);
+  a.scale = scale;
+  a.ws = ws;
+  a.cpt = p.cpr * uint32_t(p.rows);
+  a.nchunks = uint64_t(p.batch) * a.cpt;
+  a.cph = make_fastdiv(p.cpr);
+  a.used = 0;
+  a.ir = IntRange{p.qmin, p.qmax};
+  uint64_t used;
+  switch (p.fmt) {
+    case F_INT8: used = head_fmt<F_INT8>(p, a, st); break;
+    case F_INT4: used = head_fmt<F_INT4>(p, a, st); break;
+    default: used = head_fmt<F_FP8>(p, a, st); break;
+  }
+  int64_t blocks = (p.rows + 7) / 8;
+  if (blocks > 65535) blocks = 65535;
+  reduce_heads_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, used / a.cpt, a.cpt, p.cpr, p.rows,
+                                                        dscale, accumulate);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, const float* scale,
                               const float* tscale, float* dscale, float* dtscale, void* dx,
                               int accumulate, double* ws, cudaStream_t st) {
+  if (p.fmt != F_NVFP4 && p.gran == G_HEAD)
+    return launch_head_grad(p, x, dy, scale, dscale, dx, accumulate, ws, st);
   const bool partials = grad_needs_partials(p);
   float* out = (p.fmt == F_NVFP4 && p.mode == 1) ? dtscale : dscale;
   if (p.batch == 0) return cudaSuccess;
@@ -460,17 +626,18 @@ cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, c
   a.lg = grad_unit_lg(p);
   a.ir = IntRange{p.qmin, p.qmax};
   a.accumulate = accumulate;
-  a.nparts = partials ? grad_parts(p) : 0;
+  a.nparts = 0;
+  int nparts;
   switch (p.fmt) {
-    case F_INT8: grad_fmt<F_INT8>(p, a, st); break;
-    case F_INT4: grad_fmt<F_INT4>(p, a, st); break;
-    case F_FP8: grad_fmt<F_FP8>(p, a, st); break;
-    default: grad_fmt<F_NVFP4>(p, a, st); break;
+    case F_INT8: nparts = grad_fmt<F_INT8>(p, a, st); break;
+    case F_INT4: nparts = grad_fmt<F_INT4>(p, a, st); break;
+    case F_FP8: nparts = grad_fmt<F_FP8>(p, a, st); break;
+    default: nparts = grad_fmt<F_NVFP4>(p, a, st); break;
   }
   if (partials) {
     int64_t blocks = (p.batch + 7) / 8;
     if (blocks > 65535) blocks = 65535;
-    reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, a.nparts, p.batch, out, accumulate);
+    reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, nparts, p.batch, out, accumulate);
   }
   return cudaGetLastError();
 }

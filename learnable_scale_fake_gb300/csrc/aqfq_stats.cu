@@ -13,8 +13,9 @@
 //
 // Scale init ("QAT + DeepSpeed ZeRO-3", "Quantizer initial values": scale =
 // max|W| / 448 for FP8; the same rule with 127 / 7 / 6 for the other grids):
-// zero the outputs, atomicMax the float bits of |x| (non-negative floats
-// order like their bit patterns) per unit, then divide in place.
+// per-block and per-group scales are reduced by shuffles and stored directly;
+// the other units zero their outputs, atomicMax the float bits of |x|
+// (non-negative floats order like their bit patterns), then divide in place.
 #include "aqfq_internal.h"
 
 namespace aqfq {
@@ -130,7 +131,43 @@ struct InitArgs {
   uint32_t cpb;
   FastDiv cpr;
   int lg;
+  float qmax;
 };
+
+// Units of 1 << lg aligned lanes (NVFP4 blocks, groups): butterfly max, the
+// first lane of the unit stores amax / qmax.  The NVFP4 tensor amax still goes
+// through one atomicMax per warp.
+template <bool NVFP4>
+__global__ void __launch_bounds__(kThreads) amax_direct_kernel(const InitArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int width = 1 << a.lg;
+  float* scale = reinterpret_cast<float*>(a.sbits);
+  for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
+    const uint64_t base = (uint64_t)b * a.cpb;
+    uint32_t tmax = 0;
+    for (uint64_t c0 = (uint64_t)blockIdx.x * kThreads; c0 < a.cpb;
+         c0 += (uint64_t)gridDim.x * kThreads) {
+      const uint64_t c = c0 + threadIdx.x;
+      uint32_t am = 0;
+      if (c < a.cpb) {
+        uint32_t w[8];
+        ld_stream(a.x + (base + c) * 32, w);
+        am = __float_as_uint(chunk_amax(w));
+      }
+      tmax = max(tmax, am);
+      if (scale) {
+        for (int off = 1; off < width; off <<= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+        if (c < a.cpb && (lane & (width - 1)) == 0)
+          scale[(base + c) >> a.lg] = __fdiv_rn(__uint_as_float(am), a.qmax);
+      }
+    }
+    if constexpr (NVFP4) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tmax = max(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, off));
+      if (lane == 0) atomicMax(a.tbits + b, tmax);
+    }
+  }
+}
 
 template <int GRAN, bool NVFP4>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const InitArgs a) {
@@ -196,10 +233,16 @@ cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, floa
   const uint64_t cpt = uint64_t(H) * uint64_t(D / 16);
   const uint64_t nchunks = uint64_t(T) * cpt;
   if (nchunks > 0) {
-    // threads used: a multiple of the chunks per token, about 8 CTAs per SM
-    uint64_t want = uint64_t(sm_count()) * 8 * kThreads;
+    // threads used: one wave of the kernel's resident CTAs, as a multiple of
+    // the chunks per token
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, observer_reduce, kThreads, 0) !=
+            cudaSuccess || occ < 1)
+      occ = 1;
+    uint64_t want = uint64_t(sm_count()) * occ * kThreads;
     if (want > nchunks) want = nchunks;
-    uint64_t used = (want + cpt - 1) / cpt * cpt;
+    uint64_t used = want / cpt * cpt;
+    if (used < cpt) used = cpt;
     const uint64_t blocks = (used + kThreads - 1) / kThreads;
     observer_reduce<<<(unsigned)blocks, kThreads, 0, st>>>(
         static_cast<const uint8_t*>(x), nchunks, (uint32_t)cpt, make_fastdiv((uint32_t)(D / 16)),
@@ -220,6 +263,8 @@ cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, flo
                               cudaStream_t st) {
   const bool nvfp4 = p.fmt == F_NVFP4;
   const bool dyn = nvfp4 && p.mode == 1;
+  // per-block / per-group scales are written directly, the others through atomics
+  const bool direct = nvfp4 || p.gran == G_GROUP;
   int64_t nunit;
   if (nvfp4) nunit = dyn ? 0 : p.batch * int64_t(p.cpb);
   else if (p.gran == G_TENSOR) nunit = p.batch;
@@ -227,7 +272,8 @@ cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, flo
   else if (p.gran == G_HEAD) nunit = p.rows;
   else nunit = p.batch * p.rows * (p.K / p.group);
   cudaError_t e;
-  if (nunit > 0 && (e = cudaMemsetAsync(scale, 0, size_t(nunit) * 4, st)) != cudaSuccess) return e;
+  if (!direct && nunit > 0 && (e = cudaMemsetAsync(scale, 0, size_t(nunit) * 4, st)) != cudaSuccess)
+    return e;
   if (nvfp4 && p.batch > 0 && (e = cudaMemsetAsync(tscale, 0, size_t(p.batch) * 4, st)) != cudaSuccess)
     return e;
   if (p.batch > 0 && p.cpb > 0) {
@@ -243,11 +289,14 @@ cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, flo
     if (!nvfp4 && p.gran == G_GROUP) {
       while ((16 << a.lg) < p.group) ++a.lg;
     }
+    a.qmax = nvfp4 ? 6.0f : (p.fmt == F_FP8 ? 448.0f : p.qmax);
     uint64_t gx = (uint64_t(p.cpb) + kThreads - 1) / kThreads;
     if (gx > 0x7FFFFFFFull) gx = 0x7FFFFFFFull;
     dim3 grid((unsigned)gx, (unsigned)(p.batch < 65535 ? p.batch : 65535), 1);
     if (nvfp4) {
-      amax_kernel<G_GROUP, true><<<grid, kThreads, 0, st>>>(a);
+      amax_direct_kernel<true><<<grid, kThreads, 0, st>>>(a);
+    } else if (direct) {
+      amax_direct_kernel<false><<<grid, kThreads, 0, st>>>(a);
     } else {
       switch (p.gran) {
         case G_TENSOR: amax_kernel<G_TENSOR, false><<<grid, kThreads, 0, st>>>(a); break;
@@ -258,7 +307,7 @@ cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, flo
     }
   }
   const float qmax = nvfp4 ? 6.0f : (p.fmt == F_FP8 ? 448.0f : p.qmax);
-  if (nunit > 0) divide_in_place<<<small_grid(nunit), 256, 0, st>>>(scale, nunit, qmax);
+  if (!direct && nunit > 0) divide_in_place<<<small_grid(nunit), 256, 0, st>>>(scale, nunit, qmax);
   if (nvfp4 && p.batch > 0)
     divide_in_place<<<small_grid(p.batch), 256, 0, st>>>(tscale, p.batch, 448.0f * 6.0f);
   return cudaGetLastError();

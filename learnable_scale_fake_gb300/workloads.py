@@ -265,6 +265,33 @@ def observer_fp8(dev, seed=0):
     return wl
 
 
+def head_fp8_learned(dev, seed=0):
+    """Per-head FP8 E4M3 fake-quant of attention / KV activations with a learnable
+    per-head scale: forward, per-head scale gradient and STE input gradient."""
+    d = synth.cfg5(dev, seed)
+    x = d["act"]
+    T, H, D = x.shape
+    dy = synth.normal_bf16((T, H, D), 1.0, seed + 1, dev)
+    sp = Q(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    s = torch.empty(H, device=dev)
+    aqfq.aqfq_scale_init(sp, x, s, None)
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    ds = torch.empty(H, device=dev)
+    ws = torch.empty(max(1, aqfq.aqfq_scale_grad_workspace_bytes(sp, T, H, D) // 8),
+                     dtype=torch.float64, device=dev)
+    n = x.numel()
+    wl = Workload("head_fp8_learned", "per-head learnable FP8 QDQ on [65536,32,128]: fwd + scale grad + dx",
+                  {"workload": "per_head_learnable_fp8", "act": [T, H, D]})
+    wl.ops = [Op("qdq_fwd per-head fp8", "fp8_head_fwd", n, 4 * n,
+                 lambda st: aqfq.aqfq_qdq_fwd(sp, x, s, None, y, stream=st)),
+              Op("scale_grad per-head fp8 (+dx)", "fp8_head_grad", n, 6 * n,
+                 lambda st: aqfq.aqfq_scale_grad(sp, x, dy, s, None, dscale=ds, dx=dx, workspace=ws,
+                                                 stream=st), 2)]
+    wl.inputs.update({"act": x, "dy": dy, "scale": s})
+    wl.outputs.update({"y": y, "dx": dx, "dscale": ds})
+    return wl
+
+
 def int8_channel(dev, seed=0):
     d = synth.cfg1(dev, seed)
     w, dy = d["w"].unsqueeze(0), d["dy"].unsqueeze(0)
@@ -285,4 +312,5 @@ def int8_channel(dev, seed=0):
 
 
 BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
-            "observer_fp8": observer_fp8, "int8_channel": int8_channel}
+            "observer_fp8": observer_fp8, "int8_channel": int8_channel,
+            "head_fp8_learned": head_fp8_learned}

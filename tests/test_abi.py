@@ -112,7 +112,11 @@ def test_grad_argument_checks(L):
     assert grad(L, NVD, scale=None, ds=None, dts=A, ws=A + 4, wsb=need) == ALIGN
     assert grad(L, NV, dy=A + 8) == ALIGN
     assert grad(L, NV, dx=A + 8) == ALIGN
-    assert grad(L, aqfq.qspec(aqfq.FP8_E4M3, aqfq.PER_HEAD)) == UNSUP
+    hd = aqfq.qspec(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    assert grad(L, hd) == WS                      # per-head sums need a workspace
+    assert aqfq.aqfq_scale_grad_workspace_bytes(hd, 1000, 4, 64) == 1000 * 16 * 8  # all tokens
+    big = aqfq.aqfq_scale_grad_workspace_bytes(hd, 100000, 4, 64)  # one wave of the device
+    assert big % (16 * 8) == 0 and 16 * 8 <= big < 100000 * 16 * 8
     assert aqfq.aqfq_scale_grad_workspace_bytes(I8, 1, 4, 64) == 0
     assert aqfq.aqfq_scale_grad_workspace_bytes(I4, 2, 8, 128) == 0
     assert aqfq.aqfq_scale_grad_workspace_bytes(F8T, 3, 4, 64) == 3 * 8

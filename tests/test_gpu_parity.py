@@ -52,6 +52,9 @@ CASES = [
      None),
     ("fp8_g32", Q(aqfq.FP8_E4M3, aqfq.PER_GROUP, group=32), (2, 27, 320), _x_normal,
      (2e-5, 2e-4), None),
+    ("fp8_head", Q(aqfq.FP8_E4M3, aqfq.PER_HEAD), (97, 6, 64), _x_normal, (2e-5, 2e-4), None),
+    ("int8_sym_head", Q(aqfq.INT8, aqfq.PER_HEAD, qmin=-127, qmax=127), (61, 5, 48), _x_normal,
+     (1e-4, 4e-4), None),
     ("nvfp4_learned", NV, (3, 45, 208), _x_t, (2e-3, 2e-2), (2e-5, 1e-4)),
     ("nvfp4_dynamic", NVD, (3, 41, 192), _x_act, None, (1e-4, 1e-2)),
 ]
@@ -108,8 +111,11 @@ def test_scale_grad(case):
     assert np.array_equal(dx, ref["dx"]), f"{np.count_nonzero(dx != ref['dx'])} dx mismatches"
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[4], CASES[8], CASES[10], CASES[11]],
-                         ids=[IDS[0], IDS[4], IDS[8], IDS[10], IDS[11]])
+ACC = [c for c in CASES if c[0] in ("int8_channel_k512", "int4_g128", "fp8_tensor", "fp8_head",
+                                    "nvfp4_learned", "nvfp4_dynamic")]
+
+
+@pytest.mark.parametrize("case", ACC, ids=[c[0] for c in ACC])
 def test_scale_grad_accumulate_and_determinism(case):
     sp = case[1]
     x, dy, scale, ts = _inputs(case, seed=20)
@@ -126,6 +132,20 @@ def test_scale_grad_accumulate_and_determinism(case):
     ds, dts, _ = gpu_grad(sp, x, dy, scale, ts, want_dx=False, accumulate_from=old)
     got = ds if ds is not None else dts
     assert_grad_close(got, old.astype(np.float64) + r, ra, extra_abs=old, what="accumulated")
+
+
+def test_per_head_grad_many_rounds():
+    """x [T, H, D] large enough that each thread of the per-head gradient walks
+    several tokens (more chunks than threads), with the STE input gradient."""
+    sp = Q(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    T, H, D = 20000, 8, 128
+    x = synth.head_normal_bf16(T, H, D, 0.1, 10.0, seed=95)
+    dy = synth.normal_bf16((T, H, D), 1.0, seed=96)
+    s = synth.loguniform_f32((H,), 2e-4, 2e-2, seed=97)
+    ds, _, dx = gpu_grad(sp, x, dy, s, None)
+    ref = oracle_grad(sp, x, dy, s, None)
+    assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
+    assert np.array_equal(dx, ref["dx"])
 
 
 def test_special_values():

@@ -70,11 +70,11 @@ def test_noalloc_matches_workspace_entry(name, sp, shape):
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     dev()
-    sp = Q(aqfq.FP8_E4M3, aqfq.PER_TENSOR)
-    # 64 batch entries x 512 partials x 8 bytes = 256 KiB > 128 KiB
-    assert aqfq.aqfq_scale_grad_workspace_bytes(sp, 64, 1024, 4096) > (128 << 10)
+    sp = Q(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    # per-head partial sums of [65536 tokens, 32 heads, 128] exceed 128 KiB
+    assert aqfq.aqfq_scale_grad_workspace_bytes(sp, 65536, 32, 128) > (128 << 10)
     L = aqfq.lib()
     A = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
-    rc = L.aqfq_scale_grad_noalloc(ctypes.byref(sp), A, A, 64, 1024, 4096, A, None, A, None, None,
+    rc = L.aqfq_scale_grad_noalloc(ctypes.byref(sp), A, A, 65536, 32, 128, A, None, A, None, None,
                                    0, None)
     assert rc == 5  # AQFQ_ERR_WORKSPACE
