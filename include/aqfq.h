@@ -120,7 +120,20 @@ typedef struct aqfq_qspec {
  *   x            device, [batch, rows, K] BF16
  *   scale        device, shaped by spec->gran (NULL only for NVFP4 dynamic)
  *   tensor_scale device, [batch] float (NVFP4), else ignored
- *   y            device, [batch, rows, K] BF16; must not overlap x
+ *   y            device, [batch, rows, K] BF16; must not overlap x.  May be
+ *                NULL when codes are requested: real-quant export, which
+ *                writes only the packed codes (and block codes).
+ * Export layouts (the codes are the deployment tensors, byte for byte):
+ *   INT4 (w4a16): codes viewed as int32 [batch, rows, K/8] hold element 8j+i
+ *     in bits 4i..4i+3 (pack-quantized order), scale per group as given;
+ *   FP8: codes are float8_e4m3fn [batch, rows, K] with the per-channel /
+ *     per-tensor float32 scale;
+ *   NVFP4: codes uint8 [batch, rows, K/2] (element 2j in the low nibble),
+ *     block_codes float8_e4m3fn [batch, rows, K/16], dequantised value
+ *     e2m1 * e4m3 * tensor_scale (a "global scale" stored as its reciprocal
+ *     by some deployment formats is 1 / tensor_scale).
+ * (AngelSlim mcore_qad article, section 3: format names map 1:1 to the
+ * deployment side's layouts; "QAT + DeepSpeed ZeRO-3": save_format=real.)
  * Limits: rows * K / 16 < 2^32 (per batch entry). */
 aqfq_status aqfq_qdq_fwd(const aqfq_qspec* spec, const void* x, int64_t batch, int64_t rows,
                          int64_t K, const float* scale, const float* tensor_scale, void* y,

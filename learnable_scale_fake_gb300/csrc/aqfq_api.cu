@@ -141,7 +141,7 @@ aqfq_status aqfq_qdq_fwd(const aqfq_qspec* spec, const void* x, int64_t batch, i
   aqfq_status s = make_problem(spec, batch, rows, K, p);
   if (s != AQFQ_OK) return s;
   const bool any = elems(p) > 0;
-  if (any && (!x || !y)) return AQFQ_ERR_NULL;
+  if (any && (!x || (!y && !codes))) return AQFQ_ERR_NULL;
   if ((s = check_scales(p, scale, tensor_scale)) != AQFQ_OK) return s;
   if (!aligned(x, 32) || !aligned(y, 32)) return AQFQ_ERR_ALIGN;
   if (codes && !aligned(codes, byte_codes(p) ? 16 : 8)) return AQFQ_ERR_ALIGN;

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
         const Divisor dv = make_divisor(s, amax);
         if (dv.fast) qdq_chunk_fast<FMT, CODES>(xw[j], dv, a.ir, yw, cw);
         else qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
-        st_256(a.y + gc * 32, yw);
+        if (a.y) st_256(a.y + gc * 32, yw);  // NULL: export of the codes only
         if constexpr (CODES) {
           if constexpr (FMT == F_INT8 || FMT == F_FP8) {
             st_128(a.codes + gc * 16, cw[0], cw[1], cw[2], cw[3]);

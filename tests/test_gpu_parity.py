@@ -353,3 +353,52 @@ def test_scale_init(case):
         assert np.array_equal(s.cpu().numpy()[:n].view(np.uint32), s_ref.view(np.uint32))
     if ts is not None:
         assert np.array_equal(ts.cpu().numpy().view(np.uint32), ts_ref.view(np.uint32))
+
+
+def test_real_quant_export_layouts():
+    """Export (y = NULL) writes the same codes as the full forward, and the
+    codes are the deployment tensors: INT4 as pack-quantized int32 words,
+    FP8 as float8_e4m3fn, NVFP4 as E2M1 nibbles + E4M3 block scales whose
+    product with the tensor scale dequantises to x_hat."""
+    d = dev()
+    # INT4 g128
+    sp = Q(aqfq.INT4, aqfq.PER_GROUP, group=128, qmin=-8, qmax=7)
+    x = synth.normal_bf16((2, 24, 256), 0.02, seed=101)
+    s = synth.loguniform_f32((2 * 24 * 2,), 2e-3, 2e-2, seed=102)
+    y, c, _ = gpu_fwd(sp, x, s, None)
+    codes = torch.empty((2, 24, 128), dtype=torch.uint8, device=d)
+    aqfq.aqfq_qdq_fwd(sp, x.to(d), s.to(d), None, None, codes)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes.cpu().numpy(), c)
+    _, c_ref, _ = oracle_fwd(sp, x, s, None)
+    words = c_ref.reshape(-1).view(np.uint32)
+    nib = c_ref.reshape(-1)
+    expect = np.zeros(words.size, np.uint64)
+    for i in range(8):  # element 8j+i in bits 4i..4i+3
+        el = ((nib[(np.arange(words.size) * 4 + i // 2)] >> (4 * (i % 2))) & 0xF).astype(np.uint64)
+        expect |= el << np.uint64(4 * i)
+    assert np.array_equal(words.astype(np.uint64), expect)
+    # FP8 per channel: codes are float8_e4m3fn values v with x_hat = bf16(v * s)
+    sp = Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL)
+    x = synth.normal_bf16((1, 16, 128), 0.02, seed=103)
+    s = synth.loguniform_f32((16,), 2e-5, 2e-4, seed=104)
+    y, c, _ = gpu_fwd(sp, x, s, None)
+    v = torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).float()
+    assert np.array_equal((v * s.view(1, 16, 1)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), y)
+    # NVFP4: e2m1 * e4m3 * g reproduces x_hat
+    x = synth.student_t_outliers_bf16((2, 8, 64), 4, 0.02, 5e-3, 20.0, seed=105)
+    sb = synth.loguniform_f32((2 * 8 * 4,), 2e-3, 2e-2, seed=106)
+    g = synth.loguniform_f32((2,), 2e-5, 1e-4, seed=107)
+    y, c, b = gpu_fwd(NV, x, sb, g)
+    codes = torch.empty((2, 8, 32), dtype=torch.uint8, device=d)
+    blk = torch.empty((2, 8, 4), dtype=torch.uint8, device=d)
+    aqfq.aqfq_qdq_fwd(NV, x.to(d), sb.to(d), g.to(d), None, codes, blk)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes.cpu().numpy(), c) and np.array_equal(blk.cpu().numpy(), b)
+    e2m1 = np.array([oracle.e2m1_decode(k) for k in range(16)])
+    lo, hi = e2m1[c & 0xF], e2m1[c >> 4]
+    qv = np.stack([lo, hi], -1).reshape(2, 8, 64)
+    bs = torch.from_numpy(b.copy()).view(torch.float8_e4m3fn).double().numpy()
+    sh = (bs * g.numpy().astype(np.float64).reshape(2, 1, 1)).astype(np.float32).astype(np.float64)
+    xh = (qv * np.repeat(sh, 16, axis=-1)).astype(np.float32)
+    assert np.array_equal(torch.from_numpy(xh).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), y)
