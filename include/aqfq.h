@@ -232,6 +232,32 @@ aqfq_status aqfq_minmax_scale(const float* min_in, const float* max_in, int64_t 
 aqfq_status aqfq_scale_init(const aqfq_qspec* spec, const void* x, int64_t batch, int64_t rows,
                             int64_t K, float* scale, float* tensor_scale, void* stream);
 
+/* Fused NVFP4 weight fake-quant + grouped GEMM (nvfp4a16: NVFP4 weights, BF16
+ * activations).  For each expert e and each row m of x with
+ * m_offsets[e] <= m < m_offsets[e+1]:
+ *     y[m, n] = sum_k x[m, k] * w_hat_e[n, k]
+ * where w_hat_e is the NVFP4 fake-quant of w[e] with learned block scales and
+ * the expert's tensor scale, bit for bit as aqfq_grouped_qdq computes it; the
+ * fake-quantized weight is formed in shared memory and never written to
+ * device memory.  Products accumulate in FP32 on the tensor cores (tcgen05);
+ * y is rounded to BF16.
+ * Source: AngelSlim mcore_qad article, section 2.4 (vectorised fake-quant of
+ * the whole expert stack, then one grouped GEMM for every expert) and section
+ * 3 (format nvfp4a16).
+ *   x            device, [total_m, K] BF16, rows grouped by expert
+ *   m_offsets    device int32 [E + 1]: 0 = m_offsets[0] <= ... <= m_offsets[E]
+ *                = total_m (the kernel clamps them to [0, total_m])
+ *   w            device, [E, N, K] BF16;  scale [E, N, K/16] f32;
+ *   tensor_scale [E] f32;  y  device, [total_m, N] BF16
+ *   error_flag   optional device int32, set to 1 if a pipeline wait of the
+ *                kernel timed out (y is then incomplete); never cleared
+ * Limits: N % 128 == 0, K % 64 == 0, K > 0, (total_m + 127) / 128 + E <= 65535;
+ * x, w, y 32-byte aligned.  Allocates nothing; asynchronous on `stream`. */
+aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_offsets, int64_t total_m,
+                                  const void* w, const float* scale, const float* tensor_scale,
+                                  int64_t E, int64_t N, int64_t K, void* y, int32_t* error_flag,
+                                  void* stream);
+
 /* Static text for a status code. */
 const char* aqfq_status_string(aqfq_status status);
 

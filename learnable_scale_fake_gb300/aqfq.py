@@ -27,7 +27,8 @@ STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_AL
           4: "AQFQ_ERR_UNSUPPORTED", 5: "AQFQ_ERR_WORKSPACE", 6: "AQFQ_ERR_CUDA"}
 
 # every symbol include/aqfq.h declares
-EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_scale_grad", "aqfq_scale_grad_noalloc",
+EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_grouped_qdq_gemm", "aqfq_scale_grad",
+           "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
            "aqfq_scale_init", "aqfq_status_string", "aqfq_version")
 
@@ -63,6 +64,7 @@ def lib():
             sig = {
                 "aqfq_qdq_fwd": (i32, [S, P, i64, i64, i64, P, P, P, P, P, P]),
                 "aqfq_grouped_qdq": (i32, [S, P, i64, i64, i64, P, P, P, P, P, P]),
+                "aqfq_grouped_qdq_gemm": (i32, [P, P, i64, P, P, P, i64, i64, i64, P, P, P]),
                 "aqfq_scale_grad": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P, sz, P]),
                 "aqfq_scale_grad_noalloc": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P]),
                 "aqfq_scale_grad_workspace_bytes": (sz, [S, i64, i64, i64]),
@@ -144,6 +146,21 @@ def aqfq_grouped_qdq(spec, w, scale, tensor_scale, y, codes=None, block_codes=No
                                 _ptr(tensor_scale), _ptr(y), _ptr(codes), _ptr(block_codes),
                                 _stream(stream))
     _check("aqfq_grouped_qdq", st)
+
+
+def aqfq_grouped_qdq_gemm(x, m_offsets, w, scale, tensor_scale, y, error_flag=None, stream=None):
+    """y[m] = x[m] @ w_hat[e].T for the rows m of expert e (m_offsets int32 [E+1])."""
+    _bf16(x, "x"), _bf16(w, "w"), _bf16(y, "y"), _f32(scale, "scale")
+    _f32(tensor_scale, "tensor_scale")
+    if m_offsets.dtype != torch.int32 or (error_flag is not None and error_flag.dtype != torch.int32):
+        raise TypeError("m_offsets and error_flag must be int32")
+    if w.dim() != 3 or x.dim() != 2:
+        raise ValueError("x must be [total_m, K] and w [E, N, K]")
+    E, N, K = w.shape
+    st = lib().aqfq_grouped_qdq_gemm(_ptr(x), _ptr(m_offsets), x.shape[0], _ptr(w), _ptr(scale),
+                                     _ptr(tensor_scale), E, N, K, _ptr(y), _ptr(error_flag),
+                                     _stream(stream))
+    _check("aqfq_grouped_qdq_gemm", st)
 
 
 def aqfq_scale_grad_workspace_bytes(spec, batch, rows, K) -> int:

@@ -239,3 +239,28 @@ def scale_init(sp: Spec, x: np.ndarray):
     if rc:
         raise ValueError("oracle scale_init rejected the arguments")
     return scale, ts
+
+
+def grouped_qdq_gemm(x: np.ndarray, m_offsets, w: np.ndarray, scale, tensor_scale):
+    """Reference of the fused NVFP4 fake-quant + grouped GEMM: w_hat from the
+    oracle's NVFP4 forward, then y[m] = x[m] . w_hat[e] in double for the rows of
+    each expert (a library matmul serves as the contraction step).
+    x: uint16 [M, K] BF16 bits; w: uint16 [E, N, K]; returns (y, sum_k |x w_hat|)
+    as float64 [M, N]."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    E, N, K = w.shape
+    M = x.shape[0]
+    sp = spec(NVFP4, PER_GROUP, 16)
+    wh, _, _ = qdq_fwd(sp, w, scale, tensor_scale)
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wf = (wh.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    y = np.zeros((M, N), np.float64)
+    a = np.zeros((M, N), np.float64)
+    off = [int(v) for v in m_offsets]
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        if hi > lo:
+            y[lo:hi] = xf[lo:hi] @ wf[e].T
+            a[lo:hi] = np.abs(xf[lo:hi]) @ np.abs(wf[e]).T
+    return y, a

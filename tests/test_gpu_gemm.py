@@ -1,0 +1,85 @@
+"""Fused NVFP4 weight fake-quant + grouped GEMM (tcgen05) against the oracle.
+
+Exactness of the in-kernel fake-quant: with one-hot activation rows, every
+output is a single weight element times 1 (exact in any summation order), so
+y must equal the oracle's w_hat bit for bit.  General inputs: FP32
+accumulation of K products (each exact: BF16 x BF16) then rounding to BF16:
+|y - ref| <= 2^-8 |ref| + K 2^-24 sum_k |x w_hat| (a bound, not a fit)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from learnable_scale_fake_gb300 import aqfq, synth
+from paritylib import bits, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(E, N, K, sizes, seed, onehot=False):
+    w = synth.student_t_outliers_bf16((E, N, K), 4, 0.02, 5e-3, 20.0, seed)
+    s = synth.loguniform_f32((E * N * K // 16,), 2e-3, 2e-2, seed + 1)
+    g = synth.loguniform_f32((E,), 2e-5, 1e-4, seed + 2)
+    M = int(sum(sizes))
+    if onehot:
+        gen = torch.Generator().manual_seed(seed + 3)
+        cols = torch.randint(0, K, (M,), generator=gen)
+        x = torch.zeros((M, K), dtype=torch.bfloat16)
+        x[torch.arange(M), cols] = 1.0
+    else:
+        x = synth.normal_bf16((max(M, 1), K), 1.0, seed + 3)[:M]
+    off = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]), dtype=torch.int32)
+    return x, off, w, s, g
+
+
+def _run(x, off, w, s, g):
+    d = dev()
+    E, N, K = w.shape
+    y = torch.full((x.shape[0], N), float("nan"), dtype=torch.bfloat16, device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    aqfq.aqfq_grouped_qdq_gemm(x.to(d).contiguous(), off.to(d), w.to(d), s.to(d), g.to(d), y, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "a pipeline wait timed out"
+    return y.cpu()
+
+
+def test_gemm_single_tile_onehot_exact():
+    x, off, w, s, g = _inputs(1, 128, 64, [128], 200, onehot=True)
+    y = _run(x, off, w, s, g)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), s.numpy(), g.numpy())
+    assert np.array_equal(bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("E,N,K,sizes", [(3, 256, 128, [128, 200, 57]), (4, 384, 512, [0, 300, 1, 130])])
+def test_gemm_onehot_exact_ragged(E, N, K, sizes):
+    x, off, w, s, g = _inputs(E, N, K, sizes, 210 + E, onehot=True)
+    y = _run(x, off, w, s, g)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), s.numpy(), g.numpy())
+    yb, rb = bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16))
+    assert np.array_equal(yb, rb), f"{np.count_nonzero(yb != rb)} of {yb.size} differ"
+
+
+@pytest.mark.parametrize("E,N,K,sizes", [(1, 128, 64, [77]), (5, 256, 1024, [256, 0, 129, 64, 383]),
+                                         (2, 128, 2048, [300, 212])])
+def test_gemm_random_within_bound(E, N, K, sizes):
+    x, off, w, s, g = _inputs(E, N, K, sizes, 230 + E, onehot=False)
+    y = _run(x, off, w, s, g).double().numpy()
+    ref, absref = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), s.numpy(), g.numpy())
+    tol = 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -24 * absref
+    err = np.abs(y - ref)
+    assert np.all(err <= tol), f"worst excess {(err - tol).max()} at {np.unravel_index(np.argmax(err - tol), err.shape)}"
+    # typical error is far below the bound
+    rel = err / np.maximum(np.abs(ref), 1e-30)
+    assert np.median(rel) < 2.0 ** -8
+
+
+def test_gemm_argument_checks():
+    d = dev()
+    x = torch.zeros((16, 64), dtype=torch.bfloat16, device=d)
+    w = torch.zeros((1, 96, 64), dtype=torch.bfloat16, device=d)  # N % 128 != 0
+    off = torch.tensor([0, 16], dtype=torch.int32, device=d)
+    s = torch.ones(96 * 4, device=d)
+    g = torch.ones(1, device=d)
+    y = torch.empty((16, 96), dtype=torch.bfloat16, device=d)
+    with pytest.raises(aqfq.AqfqError):
+        aqfq.aqfq_grouped_qdq_gemm(x, off, w, s, g, y)

@@ -419,3 +419,30 @@ def test_scale_init_closed_forms():
     assert sb[0] == np.float32(1.75 / 6) and sb[1] == 0 and sb[16 + 1] == np.float32(0.5 / 6)
     _, gd = O.scale_init(O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK), xb)
     assert gd[0] == g[0]
+
+
+def test_grouped_gemm_reference_pins():
+    """The oracle's fused-GEMM reference: one-hot rows return rows of w_hat;
+    a tiny case equals a brute-force triple loop over the oracle's w_hat."""
+    E, N, K = 2, 4, 32
+    w = bits(synth.normal_bf16((E, N, K), 0.02, seed=61))
+    s = synth.loguniform_f32((E * N * K // 16,), 2e-3, 2e-2, seed=62).numpy()
+    g = np.array([3e-5, 6e-5], np.float32)
+    wh, _, _ = O.qdq_fwd(O.spec(O.NVFP4, O.PER_GROUP, group=16), w, s, g)
+    whf = f32_of_bits(wh).astype(np.float64)
+    off = np.array([0, 3, 5])
+    x = np.zeros((5, K), np.float32)
+    cols = [0, 7, 31, 16, 2]
+    x[np.arange(5), cols] = 1.0
+    y, a = O.grouped_qdq_gemm(bf16_bits_of(x.reshape(-1)).reshape(5, K), off, w, s, g)
+    for m, c in enumerate(cols):
+        e = 0 if m < 3 else 1
+        assert np.array_equal(y[m], whf[e, :, c])
+    xr = f32_of_bits(bits(synth.normal_bf16((5, K), 1.0, seed=63))).astype(np.float64)
+    y, a = O.grouped_qdq_gemm(bf16_bits_of(xr.reshape(-1)).reshape(5, K), off, w, s, g)
+    for m in range(5):
+        e = 0 if m < 3 else 1
+        for n in range(N):
+            t = [xr[m, k] * whf[e, n, k] for k in range(K)]
+            assert abs(y[m, n] - sum(t)) <= 1e-12 * sum(abs(v) for v in t)
+            assert abs(a[m, n] - sum(abs(v) for v in t)) <= 1e-12 * a[m, n]
