@@ -55,6 +55,16 @@ def parse():
 # peaks, clocks, profile summaries
 # ---------------------------------------------------------------------------------------
 
+def tensor_peak():
+    """Measured dense BF16 tensor throughput (burst: the kernel is timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -186,6 +196,8 @@ def _oracle_jobs(name, inputs):
     if name == "int8_channel":
         return [("w", flat(inputs["w"]).reshape(-1, 16, 512), flat(inputs["dy"]).reshape(-1, 16, 512),
                  O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), 8.0)], "leading units of 16 rows"
+    if name == "grouped_nvfp4_gemm":
+        return [("gemm", inputs["w"], None, "gemm", 0.0)], "experts (with their routed rows)"
     if name == "head_fp8_learned":
         return [("act", inputs["act"], inputs["dy"], O.spec(O.FP8_E4M3, O.PER_HEAD), 10.0)], \
             "leading tokens"
@@ -204,6 +216,17 @@ def oracle_run(name, inputs, k):
     secs = 0.0
     for nm, x, dy, sp, bpe in jobs:
         kk = min(k, x.shape[0])
+        if sp == "gemm":  # fused fake-quant GEMM: the first kk experts and their rows
+            off = [int(v) for v in inputs["m_offsets"][: kk + 1]]
+            xs = synth.bf16_bits(inputs["x"][: off[-1]])
+            w = synth.bf16_bits(inputs["w"][:kk])
+            sc, ts = O.scale_init(O.spec(O.NVFP4, O.PER_GROUP, group=16), w)
+            t0 = time.perf_counter()
+            O.grouped_qdq_gemm(xs, off, w, sc, ts)
+            secs += time.perf_counter() - t0
+            nbytes += 2 * off[-1] * w.shape[1] * w.shape[2]  # FLOPs
+            elems += off[-1] * w.shape[1]
+            continue
         xb = synth.bf16_bits(x[:kk])
         if sp is None:  # observer + scale + per-head E4M3 QDQ
             t0 = time.perf_counter()
@@ -241,6 +264,22 @@ def oracle_pick(name, inputs, target_s):
         k = min(limit, max(k + 1, int(k * min(4.0, 0.75 * target_s / max(res[2], 1e-3)))))
 
 
+def _gemm_sample_inputs(experts=4):
+    """CPU inputs for the oracle leg of the fused GEMM workload: the first
+    experts of the routed problem (same shapes and distributions)."""
+    import torch
+
+    from learnable_scale_fake_gb300 import synth
+
+    E, N, K = synth.CFG3_GATE_UP
+    counts = synth.routing_counts(E, 8192 * 8, 7)[:experts]
+    off = torch.zeros(experts + 1, dtype=torch.int64)
+    off[1:] = torch.cumsum(counts, 0)
+    return {"x": synth.normal_bf16((int(off[-1]), K), 1.0, 1),
+            "w": synth.student_t_outliers_bf16((experts, N, K), 4, 0.02, 5e-4, 20.0, 0),
+            "m_offsets": off}
+
+
 def reference_arm(args):
     """--impl reference: the oracle, as it stands, on the host cores.  Inputs come
     from the seeded generators directly; nothing of the CUDA library runs."""
@@ -253,7 +292,8 @@ def reference_arm(args):
            "int4_fp8": lambda: synth.cfg4("cpu"), "int8_channel": lambda: synth.cfg1("cpu"),
            "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)},
            "head_fp8_learned": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0),
-                                        "dy": synth.normal_bf16((4096, 32, 128), 1.0, 1)}}
+                                        "dy": synth.normal_bf16((4096, 32, 128), 1.0, 1)},
+           "grouped_nvfp4_gemm": _gemm_sample_inputs}
     inputs = gen[args.workload]()
     # the whole run (warm-up + timed steps) takes about a minute of oracle time
     per_step = 60.0 / max(1, args.steps + args.warmup)
@@ -265,17 +305,21 @@ def reference_arm(args):
             runs.append(r)
     tb = sum(r[0] for r in runs)
     ts = sum(r[2] for r in runs)
-    value = tb / ts / 1e9
+    gemm = args.workload == "grouped_nvfp4_gemm"
+    unit = "TFLOP/s" if gemm else "GB/s"
+    value = tb / ts / (1e12 if gemm else 1e9)
     threads = oracle.num_threads()
     line = {
-        "impl": "reference", "metric": "fake-quant fwd+scale-grad algorithmic HBM GB/s",
-        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "impl": "reference",
+        "metric": ("fused NVFP4 fake-quant + grouped GEMM TFLOP/s" if gemm
+                   else "fake-quant fwd+scale-grad algorithmic HBM GB/s"),
+        "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * ts / len(runs), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "sample": desc},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": desc + ", fwd + scale grad"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -369,20 +413,42 @@ def main():
     step_ms = (sum(op_ms) if flush is not None else region_ms / args.steps)
     step_ms = max_over_ranks(step_ms, dist, device)
 
-    bytes_step = wl.bytes_per_step
-    value = world * bytes_step / (step_ms * 1e-3) / 1e9
+    bytes_step = wl.bytes_per_step  # FLOPs per step for a contraction workload
+    flops_kind = getattr(wl, "flops", None) is not None
+    scale_unit = 1e12 if flops_kind else 1e9
+    value = world * bytes_step / (step_ms * 1e-3) / scale_unit
     gelem = world * wl.elems_per_step / (step_ms * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
+    if flops_kind:
+        peak, peak_kind = tensor_peak()
+    else:
+        peak, peak_kind = hbm_peak()
 
     dom = max(range(nops), key=lambda i: op_ms[i])
     dom_op = wl.ops[dom]
-    achieved = dom_op.bytes / (op_ms[dom] * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": dom_op.kernel, "op": dom_op.name,
-            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
-            if peak_kind == "measured" else "fallback",
+    achieved = dom_op.bytes / (op_ms[dom] * 1e-3) / scale_unit
+    roof = {"bound": "tensor" if flops_kind else "hbm", "kernel": dom_op.kernel, "op": dom_op.name,
+            "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s" if flops_kind else "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": (f"{peak_kind} (MEASURED_PEAKS {'bf16_tflops' if flops_kind else 'hbm_gbs'})"
+                            if peak_kind == "measured" else "fallback"),
             "traffic": stored_traffic(dom_op.name),
-            "algorithmic_bytes_per_launch": dom_op.bytes}
+            "algorithmic_bytes_per_launch" if not flops_kind else "flops_per_launch": dom_op.bytes}
+    # the same computation done the unfused way (reference path, for comparison)
+    unfused = None
+    for rop in getattr(wl, "reference_ops", []):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                rop.run(stream)
+            torch.cuda.synchronize()
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(stream)
+            for _ in range(5):
+                rop.run(stream)
+            r1.record(stream)
+        torch.cuda.synchronize()
+        rms = r0.elapsed_time(r1) / 5
+        unfused = {"op": rop.name, "ms": round(rms, 4),
+                   "value": round(rop.bytes / (rms * 1e-3) / scale_unit, 1)}
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -403,7 +469,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, device)
-        e2e = {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(world * bytes_step / (e2e_ms * 1e-3) / scale_unit, 2),
+               "unit": "TFLOP/s" if flops_kind else "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 3),
                "steps": n_e2e, "pipelined_slices": len(getattr(wl, "slices", None) or [])}
 
@@ -414,25 +481,29 @@ def main():
 
         k, _, desc = oracle_pick(args.workload, wl.inputs, target_s=20.0)
         nbytes, elems, secs = oracle_run(args.workload, wl.inputs, k)
-        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+        cpu = {"value": round(nbytes / secs / scale_unit, 6), "unit": "TFLOP/s" if flops_kind else "GB/s",
                "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": desc + ", fwd + scale grad", "seconds": round(secs, 2),
+               "sample": desc, "seconds": round(secs, 2),
                "gelem_per_s": round(elems / secs / 1e9, 5)}
 
     if rank == 0:
+        metric = ("fused NVFP4 fake-quant + grouped GEMM TFLOP/s" if flops_kind
+                  else "fake-quant fwd+scale-grad algorithmic HBM GB/s")
         line = {
-            "metric": "fake-quant fwd+scale-grad algorithmic HBM GB/s", "value": round(value, 1),
-            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "metric": metric, "value": round(value, 1),
+            "unit": "TFLOP/s" if flops_kind else "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup,
             "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "storage": "bf16", "data": "synthetic",
             "config": dict(wl.config, l2=("flushed between steps (256 MiB write)" if small
                                           else "inputs larger than L2"),
                            parallelism=f"replicas x{world}"),
             "gelem_per_s": round(gelem, 2),
-            "pct_hbm_measured": round(100 * value / world / peak, 1),
-            "pct_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+            "pct_of_peak": round(100 * value / world / peak, 1),
+            "pct_hbm_nominal_8tbs": (None if flops_kind else
+                                     round(100 * value / world / NOMINAL_HBM_GBS, 1)),
             "per_op_ms": {op.name: round(op_ms[i], 4) for i, op in enumerate(wl.ops)},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "unfused_path": unfused,
             "gpu_launches": args.steps * sum(op.launches for op in wl.ops),
             "clocks": clk,
         }

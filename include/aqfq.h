@@ -251,7 +251,7 @@ aqfq_status aqfq_scale_init(const aqfq_qspec* spec, const void* x, int64_t batch
  *   tensor_scale [E] f32;  y  device, [total_m, N] BF16
  *   error_flag   optional device int32, set to 1 if a pipeline wait of the
  *                kernel timed out (y is then incomplete); never cleared
- * Limits: N % 128 == 0, K % 64 == 0, K > 0, (total_m + 127) / 128 + E <= 65535;
+ * Limits: N % 128 == 0, K % 64 == 0, K > 0, (total_m + 511) / 512 + E <= 65535;
  * x, w, y 32-byte aligned.  Allocates nothing; asynchronous on `stream`. */
 aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_offsets, int64_t total_m,
                                   const void* w, const float* scale, const float* tensor_scale,

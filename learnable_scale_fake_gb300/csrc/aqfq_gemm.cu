@@ -6,16 +6,22 @@
 // fake-quantized, then one grouped GEMM computes every expert; here the
 // fake-quantized weight tile is made in shared memory and never written to HBM).
 //
-// One CTA computes a 128 x 128 output tile of one expert, K in steps of 64:
-//   warp 0      TMA producer: X tile [128 rows, 64] -> shared (128-byte swizzle)
-//   warp 1      allocates 128 TMEM columns; one lane issues tcgen05.mma
-//               (kind::f16, M=128, N=128, K=16 x 4 per step) and commits
+// One CTA computes up to MT = 4 output tiles of 128 x 128 of one expert that
+// share a column tile, K in steps of 64; the fake-quantized weight tile of a
+// step feeds all of them (the fake-quant work per FLOP falls by the number of
+// row tiles):
+//   warp 0      TMA producer: X tiles [128 rows, 64] -> shared (128-byte swizzle)
+//   warp 1      allocates the 512 TMEM columns (4 FP32 accumulators of 128 x
+//               128); one lane issues tcgen05.mma (kind::f16, M=128, N=128,
+//               K=16; 4 K-slices x up to 4 row tiles per step) and commits
 //   warps 2-9   weight producers: load W chunks + block scales, fake-quantize
 //               them (the same chunk arithmetic as aqfq_qdq_fwd) and store the
 //               BF16 tile into shared memory in the 128-byte swizzle layout;
-//               warps 2-5 then run the epilogue (TMEM -> registers -> BF16 -> Y)
-// A 4-stage ring of (X, W_hat) buffers; full barriers count the TMA bytes plus
-// one arrival per producer warp, empty barriers are armed by tcgen05.commit.
+//               then the epilogue (TMEM -> registers -> BF16 -> Y), two warps
+//               per TMEM lane quarter
+// A 2-stage ring of (4 X tiles, 1 W_hat tile) = 80 KiB per stage; full barriers
+// count the TMA bytes plus one arrival per producer warp, empty barriers are
+// armed by tcgen05.commit.
 // Every wait is bounded; on a timeout the CTA drains what it issued, frees
 // its tensor memory, raises the caller's error flag and returns.
 #include <cuda.h>
@@ -31,12 +37,13 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 128, BK = 64, STAGES = 2, MT = 4;
 constexpr int kGemmThreads = 320;  // 10 warps
 constexpr int kProducerThreads = 256;
-constexpr uint32_t kTileBytes = BM * BK * 2;  // 16 KiB, both operands
-constexpr uint32_t kTmemCols = 128;
-constexpr size_t kGemmSmem = 1024 + 2 * STAGES * kTileBytes + 256;
+constexpr uint32_t kTileBytes = BM * BK * 2;             // 16 KiB, one operand tile
+constexpr uint32_t kStageA = MT * kTileBytes;            // 64 KiB of X per stage
+constexpr uint32_t kTmemCols = MT * BN;                  // 512 columns
+constexpr size_t kGemmSmem = 1024 + STAGES * (kStageA + kTileBytes) + 256;
 
 struct GemmArgs {
   const uint8_t* w;       // [E, N, K] BF16
@@ -65,8 +72,8 @@ __device__ __forceinline__ bool aborted(GemmShared* sh) {
   return *reinterpret_cast<volatile int32_t*>(&sh->abort) != 0;
 }
 
-// expert and m-tile of grid row `slot` (tiles of 128 rows, experts in order);
-// one warp, result in *e / *mt (e = -1: no work)
+// expert and row group of grid row `slot` (groups of MT x 128 rows, experts
+// in order); one warp, result in *e / *mt (e = -1: no work)
 __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int slot, int* e_out,
                           int* mt_out) {
   const int lane = threadIdx.x & 31;
@@ -78,7 +85,7 @@ __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int sl
       int64_t lo = off[e], hi = off[e + 1];
       if (lo < 0) lo = 0;
       if (hi > total_m) hi = total_m;
-      t = hi > lo ? int((hi - lo + BM - 1) / BM) : 0;
+      t = hi > lo ? int((hi - lo + MT * BM - 1) / (MT * BM)) : 0;  // groups of MT row tiles
     }
     int incl = t;
 #pragma unroll
@@ -123,9 +130,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* tiles_a = smem;
-  uint8_t* tiles_b = smem + STAGES * kTileBytes;
-  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + 2 * STAGES * kTileBytes);
+  uint8_t* tiles_a = smem;                          // [STAGES][MT][16 KiB]
+  uint8_t* tiles_b = smem + STAGES * kStageA;        // [STAGES][16 KiB]
+  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + STAGES * (kStageA + kTileBytes));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0) {
@@ -154,10 +161,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem;
 
-  const int64_t row0 = int64_t(a.off[e]) + int64_t(mt) * BM;
+  // rows [row0, row0 + rows_valid) of this expert, MT tiles at most
+  const int64_t row0 = int64_t(a.off[e]) + int64_t(mt) * MT * BM;
   int64_t rows_valid = int64_t(a.off[e + 1]) - row0;
-  if (rows_valid > BM) rows_valid = BM;
+  if (rows_valid > MT * BM) rows_valid = MT * BM;
   if (row0 + rows_valid > a.total_m) rows_valid = a.total_m - row0;
+  const int ntiles = int((rows_valid + BM - 1) / BM);  // 1..MT
   const int nt = blockIdx.x;
   const int KT = int(a.K / BK);
 
@@ -171,8 +180,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           set_abort(sh);
           break;
         }
-        mbar_arrive_expect_tx(&sh->full[s], kTileBytes);
-        tma_load_2d(tiles_a + s * kTileBytes, &tmap_x, &sh->full[s], kt * BK, int32_t(row0));
+        mbar_arrive_expect_tx(&sh->full[s], kTileBytes * ntiles);
+        for (int i = 0; i < ntiles; ++i)
+          tma_load_2d(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full[s], kt * BK,
+                      int32_t(row0 + i * BM));
         ++issued;
       }
       if (aborted(sh)) {
@@ -194,12 +205,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t sa = smem_u32(tiles_a + s * kTileBytes);
+        const uint32_t sa = smem_u32(tiles_a + s * kStageA);
         const uint32_t sb = smem_u32(tiles_b + s * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          tc_mma_f16(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
-                     (kt | kk) != 0);
+          const uint64_t db = smem_desc_sw128(sb + kk * 32);
+          for (int i = 0; i < ntiles; ++i)
+            tc_mma_f16(tmem + uint32_t(i * BN), smem_desc_sw128(sa + i * kTileBytes + kk * 32), db,
+                       idesc, (kt | kk) != 0);
         }
         tc_commit(&sh->empty[s]);
       }
@@ -265,8 +278,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-    // ---- epilogue: warps 2-5, TMEM lane quarter = warp % 4 ----
-    if (warp < 6) {
+    // ---- epilogue: TMEM lane quarter = warp % 4, two warps per quarter ----
+    {
       bool ok = true;
       if (lane == 0) {
         ok = !aborted(sh) && mbar_wait(&sh->accum, 0);
@@ -277,12 +290,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok) {
         tc_fence_after_sync();
         const int q = warp & 3;
-        const int r = q * 32 + lane;
-        uint8_t* yrow = a.y + (size_t(row0 + r) * size_t(a.N) + size_t(nt) * BN) * 2;
+        const int half = (warp - 2) >> 2;  // 0 for warps 2-5, 1 for warps 6-9
 #pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
+        for (int p = half; p < ntiles * (BN / 32); p += 2) {
+          const int i = p / (BN / 32), cc = p % (BN / 32);
+          const int r = i * BM + q * 32 + lane;  // row within the group
+          uint8_t* yrow = a.y + (size_t(row0 + r) * size_t(a.N) + size_t(nt) * BN) * 2;
           uint32_t v[32];
-          tc_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cc * 32), v);
+          tc_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(i * BN + cc * 32), v);
           tc_wait_ld();
           if (r < rows_valid) {
             uint32_t o[16];
@@ -339,7 +354,7 @@ extern "C" aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_off
   if (E < 1 || N < 0 || K < 0 || total_m < 0) return AQFQ_ERR_SHAPE;
   if (N % BN != 0 || K % BK != 0) return AQFQ_ERR_SHAPE;
   if (total_m > 0x7FFFFFFF || K > (int64_t(1) << 24) || N > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
-  const int64_t slots = (total_m + BM - 1) / BM + E;
+  const int64_t slots = (total_m + MT * BM - 1) / (MT * BM) + E;  // row groups, upper bound
   if (slots > 65535 || N / BN > 65535) return AQFQ_ERR_SHAPE;
   if (!m_offsets || !tensor_scale) return AQFQ_ERR_NULL;
   if (total_m == 0 || N == 0) return AQFQ_OK;

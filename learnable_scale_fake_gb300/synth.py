@@ -158,3 +158,12 @@ def cfg5(device="cpu", seed=0):
     """Activations [65536 tokens, 32 heads, 128] with per-head std log-uniform in [0.1, 10]."""
     T, H, D = CFG5_ACT
     return {"act": head_normal_bf16(T, H, D, 0.1, 10.0, seed, device)}
+
+
+def routing_counts(E, total, seed, skew=0.3, device="cpu"):
+    """Tokens per expert for `total` routed rows: multinomial with expert
+    popularity exp(N(0, skew^2)) (a mildly unbalanced router).  int64 [E]."""
+    g = _gen(seed, "cpu")
+    pop = torch.exp(torch.randn(E, generator=g, dtype=torch.float64) * skew)
+    idx = torch.multinomial(pop / pop.sum(), total, replacement=True, generator=g)
+    return torch.bincount(idx, minlength=E).to(device)

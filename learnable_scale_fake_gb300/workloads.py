@@ -311,6 +311,52 @@ def int8_channel(dev, seed=0):
     return wl
 
 
+def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8):
+    """MoE gate_up projection with NVFP4 fake-quantized expert weights (nvfp4a16):
+    routed activations X [tokens * topk, 2048] grouped by expert, W [128, 1536, 2048].
+    Fused: one aqfq_grouped_qdq_gemm call.  Unfused reference path: the stack's
+    QDQ (aqfq_grouped_qdq, w_hat written to HBM) then one cuBLAS GEMM per expert."""
+    E, N, K = synth.CFG3_GATE_UP
+    M = tokens * topk
+    counts = synth.routing_counts(E, M, seed + 7)
+    off = torch.zeros(E + 1, dtype=torch.int32)
+    off[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    offd = off.to(dev)
+    w = synth.student_t_outliers_bf16((E, N, K), 4, 0.02, 5e-4, 20.0, seed, dev)
+    x = synth.normal_bf16((M, K), 1.0, seed + 1, dev)
+    sp = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16)
+    s = torch.empty(E * N * K // 16, device=dev)
+    g = torch.empty(E, device=dev)
+    aqfq.aqfq_scale_init(sp, w, s, g)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty_like(y)
+    wh = torch.empty_like(w)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flops = 2 * M * N * K
+    bounds = [int(v) for v in off]
+
+    def unfused(st):
+        aqfq.aqfq_grouped_qdq(sp, w, s, g, wh, stream=st)
+        for e in range(E):
+            lo, hi = bounds[e], bounds[e + 1]
+            if hi > lo:
+                torch.matmul(x[lo:hi], wh[e].t(), out=y2[lo:hi])
+
+    wl = Workload("grouped_nvfp4_gemm",
+                  "fused NVFP4 weight fake-quant + grouped GEMM, X [65536,2048] x W [128,1536,2048]",
+                  {"workload": "grouped_nvfp4_gemm_gate_up", "x": [M, K], "w": [E, N, K],
+                   "routing": "multinomial, expert popularity exp(N(0,0.3^2))"})
+    wl.ops = [Op("fused qdq+grouped gemm", "qdq_gemm", M * N, flops,
+                 lambda st: aqfq.aqfq_grouped_qdq_gemm(x, offd, w, s, g, y, err, stream=st))]
+    wl.reference_ops = [Op("unfused: qdq stack + per-expert cuBLAS", "qdq_then_cublas", M * N, flops,
+                           unfused, 1)]
+    wl.flops = flops
+    wl.inputs.update({"x": x, "w": w, "scale": s, "tscale": g, "m_offsets": offd})
+    wl.outputs.update({"y": y})
+    wl.err = err
+    return wl
+
+
 BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
             "observer_fp8": observer_fp8, "int8_channel": int8_channel,
-            "head_fp8_learned": head_fp8_learned}
+            "head_fp8_learned": head_fp8_learned, "grouped_nvfp4_gemm": grouped_nvfp4_gemm}

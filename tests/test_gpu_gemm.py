@@ -50,7 +50,8 @@ def test_gemm_single_tile_onehot_exact():
     assert np.array_equal(bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16)))
 
 
-@pytest.mark.parametrize("E,N,K,sizes", [(3, 256, 128, [128, 200, 57]), (4, 384, 512, [0, 300, 1, 130])])
+@pytest.mark.parametrize("E,N,K,sizes", [(3, 256, 128, [128, 200, 57]), (4, 384, 512, [0, 300, 1, 130]),
+                                         (2, 128, 128, [1100, 513]), (3, 128, 64, [512, 0, 1024])])
 def test_gemm_onehot_exact_ragged(E, N, K, sizes):
     x, off, w, s, g = _inputs(E, N, K, sizes, 210 + E, onehot=True)
     y = _run(x, off, w, s, g)
