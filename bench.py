@@ -366,8 +366,8 @@ def main():
         dist.barrier()
     aqfq.lib()
 
-    if args.experts is not None and args.workload == "grouped_nvfp4":
-        wl = workloads.grouped_nvfp4(device, experts=args.experts)
+    if args.experts is not None and args.workload in ("grouped_nvfp4", "grouped_nvfp4_gemm"):
+        wl = workloads.BUILDERS[args.workload](device, experts=args.experts)
     else:
         wl = workloads.BUILDERS[args.workload](device)
     stream = torch.cuda.Stream(device)

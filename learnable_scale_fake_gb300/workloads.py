@@ -311,12 +311,15 @@ def int8_channel(dev, seed=0):
     return wl
 
 
-def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8):
+def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8, experts=None):
     """MoE gate_up projection with NVFP4 fake-quantized expert weights (nvfp4a16):
     routed activations X [tokens * topk, 2048] grouped by expert, W [128, 1536, 2048].
     Fused: one aqfq_grouped_qdq_gemm call.  Unfused reference path: the stack's
     QDQ (aqfq_grouped_qdq, w_hat written to HBM) then one cuBLAS GEMM per expert."""
     E, N, K = synth.CFG3_GATE_UP
+    if experts is not None:  # smaller profiling case: fewer experts, same tokens per expert
+        tokens = tokens * experts // E
+        E = experts
     M = tokens * topk
     counts = synth.routing_counts(E, M, seed + 7)
     off = torch.zeros(E + 1, dtype=torch.int32)
