@@ -167,3 +167,36 @@ def routing_counts(E, total, seed, skew=0.3, device="cpu"):
     pop = torch.exp(torch.randn(E, generator=g, dtype=torch.float64) * skew)
     idx = torch.multinomial(pop / pop.sum(), total, replacement=True, generator=g)
     return torch.bincount(idx, minlength=E).to(device)
+
+
+# ---- distillation logits ------------------------------------------------------------
+
+# Qwen3-sized vocabulary; 4096 positions per step
+KD_VOCAB = 151936
+KD_TOKENS = 4096
+
+
+def kd_logits(T, V, seed, device="cpu", sigma=2.0, noise=0.3, ignore=0.1, hit=0.7):
+    """Teacher logits ~ N(0, sigma^2) with, at each position, one favoured
+    token raised by U(4, 12); student logits = teacher + N(0, noise^2) (the
+    same frozen model seen through fake-quantized weights); labels: the
+    favoured token with probability `hit`, else uniform over the vocabulary,
+    and -100 (no loss) at a fraction `ignore` of positions.
+    Returns (student [T, V] BF16, teacher [T, V] BF16, labels int32 [T])."""
+    g = _gen(seed, device)
+    teacher = torch.empty((T, V), dtype=torch.bfloat16, device=device)
+    student = torch.empty_like(teacher)
+    fav = torch.randint(0, V, (T,), generator=g, device=device)
+    lift = 4.0 + 8.0 * torch.rand(T, generator=g, device=device)
+    for a, b in _chunks(T, V):
+        t = torch.randn((b - a, V), generator=g, device=device) * sigma
+        t[torch.arange(b - a, device=device), fav[a:b]] += lift[a:b]
+        teacher[a:b] = t.to(torch.bfloat16)
+        student[a:b] = (teacher[a:b].float() +
+                        torch.randn((b - a, V), generator=g, device=device) * noise).to(torch.bfloat16)
+    pick = torch.rand(T, generator=g, device=device) < hit
+    other = torch.randint(0, V, (T,), generator=g, device=device)
+    labels = torch.where(pick, fav, other)
+    labels = torch.where(torch.rand(T, generator=g, device=device) < ignore,
+                         torch.full_like(labels, -100), labels)
+    return student, teacher, labels.to(torch.int32)

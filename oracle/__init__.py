@@ -18,6 +18,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "aqfq_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "kd_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "libaqfq_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -39,11 +40,11 @@ def spec(fmt, gran, group=0, qmin=0, qmax=0, mode=SCALE_LEARNED) -> Spec:
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP if available). Returns the .so path."""
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= max(
-        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "aqfq_oracle.h"))
+        [os.path.getmtime(f) for f in _SRCS] + [os.path.getmtime(os.path.join(_HERE, "aqfq_oracle.h"))]
     ):
         return _LIB_PATH
     base = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
-            "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+            "-o", _LIB_PATH + ".tmp", *_SRCS, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -88,6 +89,9 @@ def lib():
             L.orc_scale_init.restype = ctypes.c_int
             L.orc_scale_init.argtypes = [ctypes.POINTER(Spec), P, i64, i64, i64, P, P]
             L.orc_num_threads.restype = ctypes.c_int
+            L.orc_kd_loss.restype = ctypes.c_int
+            L.orc_kd_loss.argtypes = [ctypes.c_int, P, P, P, i64, i64, ctypes.c_int32,
+                                      ctypes.c_double, ctypes.c_double, P, P, P, P, P, P]
             _lib = L
     return _lib
 
@@ -264,3 +268,34 @@ def grouped_qdq_gemm(x: np.ndarray, m_offsets, w: np.ndarray, scale, tensor_scal
             y[lo:hi] = xf[lo:hi] @ wf[e].T
             a[lo:hi] = np.abs(xf[lo:hi]) @ np.abs(wf[e]).T
     return y, a
+
+
+# ---- distillation losses -----------------------------------------------------------
+
+KD_KL, KD_RKL, KD_CAKLD, KD_MSE = 0, 1, 2, 3
+
+
+def kd_loss(kd_type, student: np.ndarray, teacher: np.ndarray, labels, topk=0, temperature=1.0,
+            grad_scale=1.0, want_grad=True):
+    """student, teacher: uint16 [T, V] BF16 bits; labels int [T] (outside [0, V)
+    = no loss).  Returns a dict: losses (3,) = means over valid positions of
+    (loss, forward KL, backward KL); tok (T, 3) per position; cond (T, 2) error
+    scales; dstudent / gmag (T, V) float64 when want_grad; topk_idx (T, K) int32
+    when topk > 0."""
+    s = _c(student, np.uint16)
+    t = _c(teacher, np.uint16)
+    lab = _c(labels, np.int32)
+    T, V = s.shape
+    if t.shape != (T, V) or lab.shape != (T,):
+        raise ValueError("shape mismatch")
+    losses = np.zeros(3, np.float64)
+    tok = np.zeros((T, 3), np.float64)
+    cond = np.zeros((T, 2), np.float64)
+    ds = np.zeros((T, V), np.float64) if want_grad else None
+    gm = np.zeros((T, V), np.float64) if want_grad else None
+    idx = np.zeros((T, topk), np.int32) if topk > 0 else None
+    rc = lib().orc_kd_loss(int(kd_type), _p(s), _p(t), _p(lab), T, V, int(topk), float(temperature),
+                           float(grad_scale), _p(losses), _p(tok), _p(cond), _p(ds), _p(gm), _p(idx))
+    if rc:
+        raise ValueError(f"oracle kd_loss rejected the arguments ({rc})")
+    return {"losses": losses, "tok": tok, "cond": cond, "dstudent": ds, "gmag": gm, "topk_idx": idx}

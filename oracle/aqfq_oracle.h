@@ -91,6 +91,20 @@ int orc_scale_init(const orc_spec* sp, const uint16_t* x, int64_t batch, int64_t
 
 int orc_num_threads(void);
 
+/* ---- distillation losses (kd_oracle.c) ----
+ * kd_type: 0 kl (forward KL), 1 rkl (reverse KL), 2 cakld, 3 mse.
+ * student, teacher: [T, V] BF16 bits; labels [T] (outside [0, V) = ignored).
+ * topk: 0 = whole vocabulary, else the teacher's top-K support (K <= V).
+ * losses[3] = means over valid positions of {loss, tau^2 fkl, tau^2 rkl};
+ * tok[T, 3] the same per position; cond[T, 2] error scales (KL family, mse);
+ * dstudent / gmag [T, V] (optional): gradient of losses[0] * grad_scale and
+ * its error scale; topk_idx [T, K] (optional, topk > 0): the support in
+ * ascending vocabulary order, -1 for ignored positions. Returns 0 on success. */
+int orc_kd_loss(int kd_type, const uint16_t* student, const uint16_t* teacher,
+                const int32_t* labels, int64_t T, int64_t V, int32_t topk, double temperature,
+                double grad_scale, double* losses, double* tok, double* cond, double* dstudent,
+                double* gmag, int32_t* topk_idx);
+
 #ifdef __cplusplus
 }
 #endif
