@@ -258,6 +258,59 @@ aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_offsets, int64
                                   int64_t E, int64_t N, int64_t K, void* y, int32_t* error_flag,
                                   void* stream);
 
+/* ---- distillation losses (QAD: the student is the fake-quantized model) ----
+ * Loss between student and teacher logits with the gradient for the student
+ * logits, without any [tokens, vocab] intermediate.
+ * Sources: AngelSlim "QAT + DeepSpeed ZeRO-3" page, table "KD variants
+ * (loss_type)" (kl = KL(teacher || student), rkl = KL(student || teacher),
+ * mse, cakld = conf * rkl + (1 - conf) * fkl with conf the teacher's
+ * probability of the label, the temperature form T^2 * KL, kl_top_K /
+ * r_kl_top_K) and its cakld formula (per position, only where the label is
+ * not -100, then the mean); AngelSlim mcore_qad article, section 2.5
+ * (distill_topk: KL on the teacher's top-k tokens only).
+ * Per position with a label in [0, V), a = teacher / tau, b = student / tau,
+ * U = every token (topk = 0) or the teacher's topk largest logits (equal
+ * values lower index first; -0 equals +0), p_t = softmax over U of a,
+ * p_s = softmax over U of b:
+ *   fkl = tau^2 sum_U p_t (log p_t - log p_s)   rkl = tau^2 sum_U p_s (log p_s - log p_t)
+ *   conf = softmax(a)[label] over the whole vocabulary
+ *   loss = fkl (AQFQ_KD_KL) | rkl (AQFQ_KD_RKL) | conf rkl + (1 - conf) fkl
+ *          (AQFQ_KD_CAKLD) | mean over the vocabulary of (s - t)^2 (AQFQ_KD_MSE)
+ * Positions whose label lies outside [0, V) (the ignore index -100 among them)
+ * carry no loss and no gradient.  losses[0..2] = the means over the valid
+ * positions of (loss, fkl, rkl) (0 when there is none).
+ *   student, teacher device [T, V] BF16, V contiguous, 16-byte aligned
+ *   labels           device int32 [T]
+ *   topk             0 = whole vocabulary, else 1 <= topk <= V
+ *   temperature      tau > 0 (1 = plain); AQFQ_KD_MSE needs tau = 1, topk = 0
+ *   grad_scale       the gradient written is grad_scale * d losses[0] / d student
+ *   losses           device float [3], written
+ *   token_loss       optional device float [T]: loss per position (0 if ignored)
+ *   dstudent         optional device [T, V] BF16: the gradient (zeros outside
+ *                    the support and at ignored positions)
+ *   topk_idx         optional device int32 [T, topk] (topk > 0 only): the
+ *                    support in ascending vocabulary order, -1 rows at ignored
+ *                    positions
+ *   workspace        device, aqfq_kd_workspace_bytes(T) bytes, 16-byte aligned
+ * Limits: V % 8 == 0, 8 <= V, V up to the shared-memory bound (about 400k on
+ * GB300: each of 8 CTAs holds 1/8 of both rows).  Arithmetic in binary32 with
+ * hardware base-2 exponentials; the tests state the error bound.
+ * Launches three kernels (count, loss, mean); asynchronous on `stream`. */
+typedef enum aqfq_kd_type {
+  AQFQ_KD_KL = 0,
+  AQFQ_KD_RKL = 1,
+  AQFQ_KD_CAKLD = 2,
+  AQFQ_KD_MSE = 3
+} aqfq_kd_type;
+
+size_t aqfq_kd_workspace_bytes(int64_t T);
+
+aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void* teacher,
+                         const int32_t* labels, int64_t T, int64_t V, int32_t topk,
+                         float temperature, float grad_scale, float* losses, float* token_loss,
+                         void* dstudent, int32_t* topk_idx, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Static text for a status code. */
 const char* aqfq_status_string(aqfq_status status);
 

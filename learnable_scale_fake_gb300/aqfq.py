@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libaqfq.so")
 INT8, INT4, FP8_E4M3, NVFP4 = 0, 1, 2, 3
 PER_TENSOR, PER_CHANNEL, PER_GROUP, PER_HEAD = 0, 1, 2, 3
 SCALE_LEARNED, SCALE_DYNAMIC_BLOCK = 0, 1
+KD_KL, KD_RKL, KD_CAKLD, KD_MSE = 0, 1, 2, 3
 
 STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_ALIGN",
           4: "AQFQ_ERR_UNSUPPORTED", 5: "AQFQ_ERR_WORKSPACE", 6: "AQFQ_ERR_CUDA"}
@@ -30,7 +31,8 @@ STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_AL
 EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_grouped_qdq_gemm", "aqfq_scale_grad",
            "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
-           "aqfq_scale_init", "aqfq_status_string", "aqfq_version")
+           "aqfq_scale_init", "aqfq_kd_loss", "aqfq_kd_workspace_bytes", "aqfq_status_string",
+           "aqfq_version")
 
 
 class QSpec(ctypes.Structure):
@@ -71,6 +73,9 @@ def lib():
                 "aqfq_observer_minmax": (i32, [P, i64, i64, i64, P, P, i32, P]),
                 "aqfq_minmax_scale": (i32, [P, P, i64, ctypes.c_float, P, P]),
                 "aqfq_scale_init": (i32, [S, P, i64, i64, i64, P, P, P]),
+                "aqfq_kd_loss": (i32, [i32, P, P, P, i64, i64, ctypes.c_int32, ctypes.c_float,
+                                       ctypes.c_float, P, P, P, P, P, sz, P]),
+                "aqfq_kd_workspace_bytes": (sz, [i64]),
                 "aqfq_status_string": (ctypes.c_char_p, [i32]),
                 "aqfq_version": (i32, []),
             }
@@ -161,6 +166,30 @@ def aqfq_grouped_qdq_gemm(x, m_offsets, w, scale, tensor_scale, y, error_flag=No
                                      _ptr(tensor_scale), E, N, K, _ptr(y), _ptr(error_flag),
                                      _stream(stream))
     _check("aqfq_grouped_qdq_gemm", st)
+
+
+def aqfq_kd_workspace_bytes(T) -> int:
+    return int(lib().aqfq_kd_workspace_bytes(int(T)))
+
+
+def aqfq_kd_loss(kd_type, student, teacher, labels, losses, workspace, topk=0, temperature=1.0,
+                 grad_scale=1.0, token_loss=None, dstudent=None, topk_idx=None, stream=None):
+    """Distillation loss of student against teacher logits [T, V] (BF16) with
+    labels int32 [T]; fills losses float32 [3] (loss, forward KL, backward KL),
+    and optionally token_loss [T], dstudent [T, V] BF16 and topk_idx int32 [T, topk].
+    workspace: a uint8 device tensor of aqfq_kd_workspace_bytes(T) bytes."""
+    _bf16(student, "student"), _bf16(teacher, "teacher"), _bf16(dstudent, "dstudent")
+    _f32(losses, "losses"), _f32(token_loss, "token_loss"), _u8(workspace, "workspace")
+    if labels.dtype != torch.int32 or (topk_idx is not None and topk_idx.dtype != torch.int32):
+        raise TypeError("labels and topk_idx must be int32")
+    if student.dim() != 2 or teacher.shape != student.shape:
+        raise ValueError("student and teacher must both be [T, V]")
+    T, V = student.shape
+    st = lib().aqfq_kd_loss(int(kd_type), _ptr(student), _ptr(teacher), _ptr(labels), T, V,
+                            int(topk), float(temperature), float(grad_scale), _ptr(losses),
+                            _ptr(token_loss), _ptr(dstudent), _ptr(topk_idx), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check("aqfq_kd_loss", st)
 
 
 def aqfq_scale_grad_workspace_bytes(spec, batch, rows, K) -> int:

@@ -158,3 +158,35 @@ def test_fastdiv_constants_exhaustive_small():
                  [rnd.randrange(0, 1 << 32) for _ in range(20)]:
             if 0 <= n < (1 << 32):
                 assert div(n, d) == n // d, (n, d)
+
+
+def kd(L, kd_type=0, s=A, t=2 * A, lab=3 * A, T=4, V=64, topk=0, tau=1.0, gs=1.0, losses=4 * A,
+       tl=None, ds=None, idx=None, ws=5 * A, wsb=1 << 20):
+    return L.aqfq_kd_loss(kd_type, s, t, lab, T, V, topk, tau, gs, losses, tl, ds, idx, ws, wsb, None)
+
+
+def test_kd_loss_host_checks(L):
+    assert kd(L, kd_type=4) == UNSUP
+    assert kd(L, kd_type=-1) == UNSUP
+    assert kd(L, V=60) == SHAPE            # V % 8
+    assert kd(L, V=0) == SHAPE
+    assert kd(L, T=-1) == SHAPE
+    assert kd(L, topk=65) == SHAPE         # topk > V
+    assert kd(L, topk=-1) == SHAPE
+    assert kd(L, tau=0.0) == SHAPE
+    assert kd(L, tau=-2.0) == SHAPE
+    assert kd(L, tau=float("inf")) == SHAPE
+    assert kd(L, gs=float("nan")) == SHAPE
+    assert kd(L, kd_type=3, topk=5) == UNSUP       # mse: no top-K
+    assert kd(L, kd_type=3, tau=2.0) == UNSUP      # mse: no temperature
+    assert kd(L, idx=6 * A) == UNSUP               # topk_idx needs topk > 0
+    assert kd(L, losses=None) == NULL
+    assert kd(L, s=None) == NULL
+    assert kd(L, lab=None) == NULL
+    assert kd(L, ws=None) == WS
+    assert kd(L, wsb=aqfq.aqfq_kd_workspace_bytes(4) - 1) == WS
+    assert kd(L, s=A + 8) == ALIGN
+    assert kd(L, ds=6 * A + 4) == ALIGN
+    assert kd(L, tl=6 * A + 2) == ALIGN
+    assert aqfq.aqfq_kd_workspace_bytes(0) == 256
+    assert aqfq.aqfq_kd_workspace_bytes(4096) >= 256 + 12 * 4096
