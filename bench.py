@@ -198,6 +198,10 @@ def _oracle_jobs(name, inputs):
                  O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), 8.0)], "leading units of 16 rows"
     if name == "grouped_nvfp4_gemm":
         return [("gemm", inputs["w"], None, "gemm", 0.0)], "experts (with their routed rows)"
+    if name in ("kd_cakld", "kd_topk"):
+        kt, k = (O.KD_CAKLD, 0) if name == "kd_cakld" else (O.KD_KL, 1000)
+        return [("kd", inputs["teacher"], inputs["student"], ("kd", kt, k, inputs["labels"]), 6.0)], \
+            "leading positions"
     if name == "head_fp8_learned":
         return [("act", inputs["act"], inputs["dy"], O.spec(O.FP8_E4M3, O.PER_HEAD), 10.0)], \
             "leading tokens"
@@ -226,6 +230,16 @@ def oracle_run(name, inputs, k):
             secs += time.perf_counter() - t0
             nbytes += 2 * off[-1] * w.shape[1] * w.shape[2]  # FLOPs
             elems += off[-1] * w.shape[1]
+            continue
+        if isinstance(sp, tuple) and sp[0] == "kd":  # distillation loss: the first kk positions
+            _, kt, topk, labels = sp
+            tb, sb = synth.bf16_bits(x[:kk]), synth.bf16_bits(dy[:kk])
+            lab = labels[:kk].cpu().numpy()
+            t0 = time.perf_counter()
+            O.kd_loss(kt, sb, tb, lab, topk=topk)
+            secs += time.perf_counter() - t0
+            nbytes += int(bpe * tb.size)
+            elems += tb.size
             continue
         xb = synth.bf16_bits(x[:kk])
         if sp is None:  # observer + scale + per-head E4M3 QDQ
@@ -280,6 +294,23 @@ def _gemm_sample_inputs(experts=4):
             "m_offsets": off}
 
 
+def _kd_sample_inputs(T=64):
+    """CPU inputs for the oracle leg of the distillation workloads: the first
+    positions of the same recipe (Qwen3-sized vocabulary)."""
+    from learnable_scale_fake_gb300 import synth
+
+    s, t, lab = synth.kd_logits(T, synth.KD_VOCAB, 0)
+    return {"student": s, "teacher": t, "labels": lab}
+
+
+def metric_name(workload, flops_kind):
+    if flops_kind:
+        return "fused NVFP4 fake-quant + grouped GEMM TFLOP/s"
+    if workload.startswith("kd_"):
+        return "distillation loss + student-logit gradient algorithmic HBM GB/s"
+    return "fake-quant fwd+scale-grad algorithmic HBM GB/s"
+
+
 def reference_arm(args):
     """--impl reference: the oracle, as it stands, on the host cores.  Inputs come
     from the seeded generators directly; nothing of the CUDA library runs."""
@@ -293,7 +324,8 @@ def reference_arm(args):
            "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)},
            "head_fp8_learned": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0),
                                         "dy": synth.normal_bf16((4096, 32, 128), 1.0, 1)},
-           "grouped_nvfp4_gemm": _gemm_sample_inputs}
+           "grouped_nvfp4_gemm": _gemm_sample_inputs,
+           "kd_cakld": _kd_sample_inputs, "kd_topk": _kd_sample_inputs}
     inputs = gen[args.workload]()
     # the whole run (warm-up + timed steps) takes about a minute of oracle time
     per_step = 60.0 / max(1, args.steps + args.warmup)
@@ -311,8 +343,7 @@ def reference_arm(args):
     threads = oracle.num_threads()
     line = {
         "impl": "reference",
-        "metric": ("fused NVFP4 fake-quant + grouped GEMM TFLOP/s" if gemm
-                   else "fake-quant fwd+scale-grad algorithmic HBM GB/s"),
+        "metric": metric_name(args.workload, gemm),
         "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * ts / len(runs), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -487,8 +518,7 @@ def main():
                "gelem_per_s": round(elems / secs / 1e9, 5)}
 
     if rank == 0:
-        metric = ("fused NVFP4 fake-quant + grouped GEMM TFLOP/s" if flops_kind
-                  else "fake-quant fwd+scale-grad algorithmic HBM GB/s")
+        metric = metric_name(args.workload, flops_kind)
         line = {
             "metric": metric, "value": round(value, 1),
             "unit": "TFLOP/s" if flops_kind else "GB/s", "n_gpus": world, "steps": args.steps,

@@ -14,18 +14,26 @@
 // averaged over the valid positions; the gradient of that mean times
 // grad_scale is written for the student logits.
 //
-// Layout of the work: one cluster of 8 CTAs per position.  CTA r holds the
-// vocabulary slice [r S, r S + S) of both rows in shared memory (loaded once
-// from HBM), so every later pass reads shared memory and HBM sees each logit
-// once and each gradient element once.  Row statistics (max and sum of
-// exponentials per row, the top-K histograms, the loss sums) are combined
-// across the cluster through distributed shared memory, always in rank
-// order, so every CTA holds bit-identical row values and results are
-// reproducible.
+// Layout of the work: one cluster of 16 CTAs per position, two CTAs per SM.
+// CTA r holds the vocabulary slice [r S, r S + S) of both rows in shared
+// memory; a bulk copy (TMA, one per tensor) brings the next position's slice
+// into the other of two buffers while the current one is processed, so HBM
+// sees each logit once and each gradient element once and stays busy through
+// the cluster barriers.  Row statistics (max and sum of exponentials), the
+// top-K histograms and the loss sums are combined across the cluster through
+// distributed shared memory, always in rank order, so every CTA holds
+// bit-identical row values and results are reproducible.
+//
+// Top-K support: 16-bit order-preserving keys of the teacher's BF16 values.
+// The K-th largest element is at least the K-th largest of the 8-element
+// vector maxima, so a histogram of vector maxima (one count per vector)
+// bounds the threshold from below; only elements above that bound are
+// counted at 12-bit resolution, then the threshold bin is resolved to the
+// exact key with a 4-bit histogram; equal keys are taken in index order.
 //
 // Numerics: logits are scaled to base-2 units (x = v * log2(e) / tau) and
-// exponentials use ex2.approx; log-sum-exp uses the row maximum.  The loss
-// is summed per element as p_t d - p_t + p_s (forward) and -p_s d - p_s + p_t
+// exponentials use ex2.approx; log-sum-exp uses the maximum.  The loss is
+// summed per element as p_t d - p_t + p_s (forward) and -p_s d - p_s + p_t
 // (reverse), d = log p_t - log p_s in nats: the added -p_t + p_s terms sum to
 // zero exactly in real arithmetic and make the sum insensitive, to first
 // order, to the rounding of the two normalisers.
@@ -35,11 +43,21 @@
 
 #include "aqfq.h"
 #include "aqfq_internal.h"
+#include "aqfq_sm100.cuh"
 
 namespace aqfq {
 namespace {
 
-constexpr int kCl = 8;          // CTAs per position (vocabulary slices)
+using sm100::smem_u32;
+
+#ifndef AQFQ_KD_CLUSTER
+#define AQFQ_KD_CLUSTER 8
+#endif
+#ifndef AQFQ_KD_NBUF
+#define AQFQ_KD_NBUF 1
+#endif
+constexpr int kCl = AQFQ_KD_CLUSTER;  // CTAs per position (vocabulary slices)
+constexpr int kNbuf = AQFQ_KD_NBUF;   // slice buffers per CTA
 constexpr int kThr = 512;       // threads per CTA
 constexpr int kWarps = kThr / 32;
 constexpr int kHist1 = 4096;    // bins: the top 12 bits of the 16-bit teacher key
@@ -50,9 +68,9 @@ struct KdArgs {
   const uint16_t* s;        // student [T, V] BF16
   const uint16_t* t;        // teacher [T, V] BF16
   const int32_t* labels;    // [T]
-  const int32_t* nvalid;    // device: number of valid positions
-  float* tok;               // workspace [T, 3]: loss, tau^2 fkl, tau^2 rkl
-  float* token_loss;        // optional [T]
+  int32_t* ws_head;         // [0]: number of valid positions, [1]: error word
+  float* part;              // workspace [T, kCl, 2]: each slice's forward / reverse KL sums
+  float* rowx;              // workspace [T, 2]: conf and the sum of (s - t)^2 of each position
   uint16_t* ds;             // optional [T, V] BF16
   int32_t* topk_idx;        // optional [T, K]
   int64_t T, V;
@@ -64,13 +82,16 @@ struct KdArgs {
 };
 
 struct __align__(16) KdShared {
-  float xbuf[2][16];        // scalar exchanges (alternating)
-  float red[kWarps][8];     // block reductions
+  uint64_t full[2];         // mbarriers of the two slice buffers
+  float xbuf[2][12];        // exchange slots (alternating)
+  float red[kWarps][12];    // block reductions
   int32_t ired[kWarps + 1];
   uint32_t hist2[16];       // low nibble of the keys in the threshold bin
   uint32_t h2all[kCl][16];  // hist2 of every rank
-  float label_x;            // teacher x at the label (owner CTA)
-  int32_t sel[8];           // threshold bin, need, key, idx_lim, ...
+  int32_t sel[8];           // threshold search results
+  int32_t err;
+  float res[10];            // the last reduction's result, for every thread
+  uint32_t bins[32];        // cluster-wide counts of 32 histogram bins
 };
 
 // ---------------------------------------------------------------------------
@@ -99,9 +120,7 @@ __device__ __forceinline__ void cluster_sync() {
 }
 __device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank) {
   uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(r)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
 __device__ __forceinline__ float ld_remote_f32(uint32_t a) {
@@ -114,29 +133,71 @@ __device__ __forceinline__ uint32_t ld_remote_u32(uint32_t a) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
   return v;
 }
-__device__ __forceinline__ uint4 ld_remote_v4(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a)
-               : "memory");
-  return v;
+
+// one bulk copy global -> this CTA's shared memory, completing on `bar`
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ---------------------------------------------------------------------------
-// small helpers
+// arithmetic helpers; f2 = a pair of binary32 values in one 64-bit register
+// (packed FP32 instructions of sm_100-class GPUs)
 // ---------------------------------------------------------------------------
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 mk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(f2 v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi2(f2 v) { return __uint_as_float(uint32_t(v >> 32)); }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float bf16f(uint32_t w, int hi) {
-  return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16));
+__device__ __forceinline__ f2 ex2x2(f2 v) { return mk2(ex2(lo2(v)), ex2(hi2(v))); }
+// a BF16 pair (element 2i in the low half) as two binary32 values
+__device__ __forceinline__ f2 bf2(uint32_t w) {
+  return mk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
-__device__ __forceinline__ uint32_t pack2(float hi, float lo) {
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// largest of the 8 BF16 values of a vector, as binary32
+__device__ __forceinline__ float vmax8(uint4 w) {
+  const uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t pack2(f2 v) {  // RNE to a BF16 pair (lo in bits 15..0)
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi2(v)), "f"(lo2(v)));
   return r;
 }
 // order-preserving 16-bit key of a BF16 value; -0 and +0 share a key
@@ -145,13 +206,15 @@ __device__ __forceinline__ uint32_t okey(uint32_t b) {
   if (b == 0x8000u) b = 0;
   return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ uint32_t word(const uint4& w, int i) {
+  return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
 }
+__device__ __forceinline__ uint32_t key_of(const uint4& w, int j) {
+  const uint32_t x = word(w, j >> 1);
+  return okey(j & 1 ? x >> 16 : x);
+}
+// key of a binary32 value that is exactly a BF16 value
+__device__ __forceinline__ uint32_t key_of_f(float f) { return okey(__float_as_uint(f) >> 16); }
 __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -175,51 +238,97 @@ __device__ __forceinline__ Online online_shfl(Online a, int d) {
   return Online{__shfl_xor_sync(0xFFFFFFFFu, a.m, d), __shfl_xor_sync(0xFFFFFFFFu, a.z, d),
                 __shfl_xor_sync(0xFFFFFFFFu, a.b, d)};
 }
-__device__ __forceinline__ Online warp_online(Online a) {
+
+// A reduction record: online states of teacher and student, two sums and one
+// integer combined by max (KMAX) or by sum.
+struct Rec {
+  Online t, s;
+  float u, v;
+  int k;
+};
+__device__ __forceinline__ Rec rec_empty() { return Rec{online_empty(), online_empty(), 0.0f, 0.0f, 0}; }
+template <bool KMAX>
+__device__ __forceinline__ Rec rec_merge(const Rec& a, const Rec& c) {
+  return Rec{online_merge(a.t, c.t), online_merge(a.s, c.s), __fadd_rn(a.u, c.u),
+             __fadd_rn(a.v, c.v), KMAX ? max(a.k, c.k) : a.k + c.k};
+}
+__device__ __forceinline__ Rec rec_shfl(const Rec& a, int d) {
+  return Rec{online_shfl(a.t, d), online_shfl(a.s, d), __shfl_xor_sync(0xFFFFFFFFu, a.u, d),
+             __shfl_xor_sync(0xFFFFFFFFu, a.v, d), __shfl_xor_sync(0xFFFFFFFFu, a.k, d)};
+}
+// xor butterfly over the warp: every lane ends with the same total (the merge
+// is symmetric bit for bit), in a fixed order
+template <bool KMAX>
+__device__ __forceinline__ Rec warp_rec(Rec a) {
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) a = online_merge(a, online_shfl(a, d));
+  for (int d = 16; d >= 1; d >>= 1) a = rec_merge<KMAX>(a, rec_shfl(a, d));
   return a;
 }
-
-// Block reduction of N sums: every thread gets the totals (fixed order).
-template <int N>
-__device__ __forceinline__ void block_sum(float (&v)[N], KdShared* sh) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < N; ++i)
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xFFFFFFFFu, v[i], d));
-  if (l == 0)
-#pragma unroll
-    for (int i = 0; i < N; ++i) sh->red[w][i] = v[i];
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    float s = 0.0f;
-    for (int k = 0; k < kWarps; ++k) s = __fadd_rn(s, sh->red[k][i]);
-    v[i] = s;
-  }
-  __syncthreads();
+__device__ __forceinline__ void rec_store(float* p, const Rec& a) {
+  p[0] = a.t.m; p[1] = a.t.z; p[2] = a.t.b; p[3] = a.s.m; p[4] = a.s.z; p[5] = a.s.b;
+  p[6] = a.u; p[7] = a.v; p[8] = __int_as_float(a.k);
+}
+__device__ __forceinline__ Rec rec_load(const float* p) {
+  return Rec{Online{p[0], p[1], p[2]}, Online{p[3], p[4], p[5]}, p[6], p[7], __float_as_int(p[8])};
 }
 
-// Block reduction of two online states (teacher, student) into totals.
-__device__ __forceinline__ void block_online2(Online& a, Online& c, KdShared* sh) {
+// Block reduction of one record per thread; every thread gets the total.
+// Warps reduce by butterfly, then warp 0 merges the warps' records.
+template <bool KMAX>
+__device__ __forceinline__ Rec block_rec(Rec a, KdShared* sh) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  a = warp_online(a);
-  c = warp_online(c);
-  if (l == 0) {
-    sh->red[w][0] = a.m; sh->red[w][1] = a.z; sh->red[w][2] = a.b;
-    sh->red[w][3] = c.m; sh->red[w][4] = c.z; sh->red[w][5] = c.b;
+  a = warp_rec<KMAX>(a);
+  if (l == 0) rec_store(sh->red[w], a);
+  __syncthreads();
+  if (w == 0) {
+    Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
+    x = warp_rec<KMAX>(x);
+    if (l == 0) rec_store(sh->res, x);
   }
   __syncthreads();
-  Online ta = online_empty(), tc = online_empty();
-  for (int k = 0; k < kWarps; ++k) {
-    ta = online_merge(ta, Online{sh->red[k][0], sh->red[k][1], sh->red[k][2]});
-    tc = online_merge(tc, Online{sh->red[k][3], sh->red[k][4], sh->red[k][5]});
+  return rec_load(sh->res);
+}
+
+// Cluster reduction of one record per CTA (thread 0's `mine`): the record goes
+// to this CTA's exchange slot `par`, the cluster synchronises, warp 0 reads
+// the kCl records (lane r from rank r) and merges them by butterfly, the same
+// way in every CTA, so all CTAs hold bit-identical totals.  k_before (if not
+// NULL) receives the sum of k over the ranks below this one.  A slot is
+// rewritten two exchanges later, after a barrier that every CTA passes only
+// once it has read the slot.
+template <bool KMAX>
+__device__ __forceinline__ Rec cluster_rec(const Rec& mine, KdShared* sh, int& par,
+                                           int* k_before = nullptr) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (threadIdx.x == 0) rec_store(sh->xbuf[par], mine);
+  cluster_sync();
+  if (w == 0) {
+    Rec x = rec_empty();
+    if (l < kCl) {
+      const uint32_t base = remote_addr(&sh->xbuf[par][0], uint32_t(l));
+      float v[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) v[i] = ld_remote_f32(base + 4u * i);
+      x = rec_load(v);
+    }
+    if (k_before) {  // exclusive prefix over the ranks below this one
+      int inc = x.k;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if (l >= d) inc += y;
+      }
+      if (uint32_t(l) == cluster_rank()) sh->res[9] = __int_as_float(inc - x.k);
+    }
+    x = warp_rec<KMAX>(x);
+    if (l == 0) rec_store(sh->res, x);
   }
-  a = ta;
-  c = tc;
   __syncthreads();
+  const Rec r = rec_load(sh->res);
+  if (k_before) *k_before = __float_as_int(sh->res[9]);
+  __syncthreads();
+  par ^= 1;
+  return r;
 }
 
 // Block-wide inclusive scan of one int per thread; returns (inclusive, total).
@@ -243,30 +352,57 @@ __device__ __forceinline__ int block_scan(int v, int& total, KdShared* sh) {
   return x + before;
 }
 
-// Exchange n <= 16 floats with the cluster: writes them to this CTA's
-// exchange slot `par`, synchronises the cluster and returns every rank's
-// values in out[rank][i].  A slot is rewritten two exchanges later, after a
-// barrier that every CTA passes only once it has read the slot.
-template <int N>
-__device__ __forceinline__ void cluster_exchange(const float (&mine)[N], float (&out)[kCl][N],
-                                                 KdShared* sh, int& par) {
-  if (threadIdx.x == 0)
+// After a cluster barrier: walking down from bin `top`, the bin at which the
+// cluster-wide count of a 4096-bin histogram reaches K, and the count above
+// that bin.  Returns false (bin 0, the whole count) when the histogram holds
+// fewer than K.  All threads call it.  Each step covers 32 bins: thread t
+// loads bin t / 16 of the step from rank t % 16 (one remote load each).
+__device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int K, int& bin,
+                                              int& above, KdShared* sh) {
+  static_assert(kThr >= 32 * kCl && kCl <= 32, "one remote load per thread per 32-bin step");
+  const int tid = threadIdx.x, j = tid / kCl, r = tid % kCl;
+  const bool part = tid < 32 * kCl;
+  int base = 0;
+  for (int b0 = top; b0 >= 0; b0 -= 32) {
+    const int b = b0 - j;
+    uint32_t c = (part && b >= 0) ? ld_remote_u32(remote_addr(hist + b, r)) : 0u;
 #pragma unroll
-    for (int i = 0; i < N; ++i) sh->xbuf[par][i] = mine[i];
-  cluster_sync();
+    for (int d = kCl / 2; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
+    if (part && r == 0) sh->bins[j] = c;
+    __syncthreads();
+    if (tid < 32) {  // one warp scans the 32 bins from the top
+      const int cj = int(sh->bins[tid]);
+      int x = cj;
 #pragma unroll
-  for (int r = 0; r < kCl; ++r) {
-    const uint32_t base = remote_addr(&sh->xbuf[par][0], r);
-#pragma unroll
-    for (int i = 0; i < N; ++i) out[r][i] = ld_remote_f32(base + 4u * i);
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+        if (tid >= d) x += y;
+      }
+      const int incl = base + x;
+      if (incl - cj < K && incl >= K) {
+        sh->sel[6] = b0 - tid;
+        sh->sel[7] = incl - cj;
+      }
+      if (tid == 31) sh->sel[1] = incl;  // running total after this step
+    }
+    __syncthreads();
+    base = sh->sel[1];
+    if (base >= K) {
+      bin = sh->sel[6];
+      above = sh->sel[7];
+      __syncthreads();
+      return true;
+    }
+    __syncthreads();
   }
-  par ^= 1;
+  bin = 0;
+  above = base;
+  return false;
 }
 
-
 // Visits the slice in index order and calls emit(local index, position) for
-// every element whose teacher key satisfies pred(local index, key); the
-// position counts those elements from 0 in index order.  All threads call it.
+// every element that satisfies pred(local index, key); the position counts
+// those elements from 0 in index order.  All threads call it.
 template <class Pred, class Emit>
 __device__ __forceinline__ void ordered_scan(const uint16_t* tsl, int nvec, Pred pred, Emit emit,
                                              KdShared* sh) {
@@ -276,10 +412,9 @@ __device__ __forceinline__ void ordered_scan(const uint16_t* tsl, int nvec, Pred
     uint32_t m8 = 0;
     if (v < nvec) {
       const uint4 w = *reinterpret_cast<const uint4*>(tsl + 8 * v);
-      const uint32_t tw[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (pred(8 * v + j, okey(j & 1 ? tw[j >> 1] >> 16 : tw[j >> 1]))) m8 |= 1u << j;
+        if (pred(8 * v + j, key_of(w, j))) m8 |= 1u << j;
     }
     const int c = __popc(m8);
     int total;
@@ -293,15 +428,20 @@ __device__ __forceinline__ void ordered_scan(const uint16_t* tsl, int nvec, Pred
   }
 }
 
-// One cluster per position (persistent over positions).  TOPK: restrict to
-// the teacher's top-K support.
-template <bool TOPK>
+// One cluster per position, persistent over positions.
+//   TOPK   restrict to the teacher's top-K support
+//   RGRAD  the gradient has a reverse-KL part (rkl, cakld): pass 1 also sums
+//          2^(x_s - m) (x_s - x_t) for the reverse KL that centres it
+//   MSE    mean squared error loss and gradient
+template <bool TOPK, bool RGRAD, bool MSE>
 __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
   extern __shared__ __align__(16) uint8_t kd_smem[];
   KdShared* sh = reinterpret_cast<KdShared*>(kd_smem);
-  uint32_t* hist1 = reinterpret_cast<uint32_t*>(kd_smem + sizeof(KdShared));
-  uint16_t* tsl = reinterpret_cast<uint16_t*>(kd_smem + sizeof(KdShared) + (TOPK ? kHist1 * 4 : 0));
-  uint16_t* ssl = tsl + a.S;
+  uint32_t* vhist = reinterpret_cast<uint32_t*>(kd_smem + sizeof(KdShared));  // vector-max bins
+  uint32_t* hist1 = vhist + (TOPK ? kHist1 : 0);                               // element bins
+  uint16_t* vbin = reinterpret_cast<uint16_t*>(hist1 + (TOPK ? kHist1 : 0));   // bin of each vector max
+  const int vbin_n = TOPK ? (a.S / 8 + 7) / 8 * 8 : 0;
+  uint16_t* buf0 = vbin + vbin_n;  // two buffers of [teacher S | student S]
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_rank();
   const int64_t v0 = int64_t(rank) * a.S;  // first vocabulary index of this slice
@@ -309,179 +449,171 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
   if (n64 > a.S) n64 = a.S;
   if (n64 < 0) n64 = 0;
   const int nvec = int(n64) >> 3;  // V % 8 == 0 and S % 8 == 0
-  const int nval = *a.nvalid;
-  const bool mse = a.type == AQFQ_KD_MSE;
-  const bool need_b = a.ds != nullptr && (a.type == AQFQ_KD_RKL || a.type == AQFQ_KD_CAKLD);
+  const uint32_t bytes = uint32_t(n64) * 2u;
+  const int64_t G = cluster_count();
+  const int nval = a.ws_head[0];
   const float ks = a.ks;
-  // gradient factors: d(tau^2 KL(s / tau)) / ds = tau dKL/db, over the mean
-  const float gsc = nval > 0 ? (mse ? a.grad_scale * 2.0f / (float(a.V) * float(nval))
+  // d(tau^2 KL(s / tau)) / ds = tau dKL/db, over the mean
+  const float gsc = nval > 0 ? (MSE ? a.grad_scale * 2.0f / (float(a.V) * float(nval))
                                     : a.grad_scale * a.tau / float(nval))
                              : 0.0f;
-  int par = 0;
+  if (tid == 0) {
+    sm100::mbar_init(&sh->full[0], 1);
+    sm100::mbar_init(&sh->full[1], 1);
+    sh->err = 0;
+    sm100::fence_barrier_init();
+  }
+  __syncthreads();
 
-  for (int64_t row = cluster_id(); row < a.T; row += cluster_count()) {
-    const int32_t label = a.labels[row];
-    const bool valid = label >= 0 && int64_t(label) < a.V;
-    const uint16_t* trow = a.t + row * a.V + v0;
-    const uint16_t* srow = a.s + row * a.V + v0;
+  auto is_valid = [&](int64_t r) {
+    const int32_t l = a.labels[r];
+    return l >= 0 && int64_t(l) < a.V;
+  };
+  auto next_valid = [&](int64_t r) -> int64_t {
+    for (; r < a.T; r += G)
+      if (is_valid(r)) return r;
+    return -1;
+  };
+  auto prefetch = [&](int64_t r, int b) {  // thread 0
+    uint16_t* tb = buf0 + size_t(b) * 2 * a.S;
+    if (bytes) {
+      sm100::mbar_arrive_expect_tx(&sh->full[b], 2u * bytes);
+      bulk_load(tb, a.t + r * a.V + v0, bytes, &sh->full[b]);
+      bulk_load(tb + a.S, a.s + r * a.V + v0, bytes, &sh->full[b]);
+    } else {
+      sm100::mbar_arrive(&sh->full[b]);  // an empty slice completes the phase at once
+    }
+  };
+  {
+    const int64_t first = next_valid(cluster_id());
+    if (first >= 0 && tid == 0) prefetch(first, 0);
+  }
+  uint32_t uses[2] = {0, 0};
+  int it = 0, par = 0;
+
+  for (int64_t row = cluster_id(); row < a.T; row += G) {
     uint16_t* drow = a.ds ? a.ds + row * a.V + v0 : nullptr;
-    if (!valid) {  // the same decision in every CTA of the cluster: no exchange
+    if (!is_valid(row)) {  // the same decision in every CTA of the cluster: no exchange
       if (drow)
         for (int v = tid; v < nvec; v += kThr) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
       if (rank == 0) {
         if (TOPK && a.topk_idx)
           for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
-        if (tid == 0) {
-          a.tok[3 * row] = a.tok[3 * row + 1] = a.tok[3 * row + 2] = 0.0f;
-          if (a.token_loss) a.token_loss[row] = 0.0f;
-        }
       }
       continue;
     }
+    const int b = kNbuf == 2 ? (it & 1) : 0;
+    ++it;
+    // every read of the other buffer (the previous position) is done: refill it
+    __syncthreads();
+    if (kNbuf == 2 && tid == 0) {
+      const int64_t after = next_valid(row + G);
+      if (after >= 0) {
+        sm100::fence_proxy_async_smem();
+        prefetch(after, b ^ 1);
+      }
+    }
     if (TOPK) {  // peers finished reading these before the last exchange of the previous row
-      for (int i = tid; i < kHist1; i += kThr) hist1[i] = 0;
+      for (int i = tid; i < 2 * kHist1; i += kThr) vhist[i] = 0;
       if (tid < 16) sh->hist2[tid] = 0;
-      __syncthreads();
     }
-    const int64_t lloc = int64_t(label) - v0;  // label's index within the slice
+    if (!sm100::mbar_wait(&sh->full[b], uses[b] & 1u)) atomicExch(&sh->err, 1);
+    ++uses[b];
+    __syncthreads();
+    const uint16_t* tsl = buf0 + size_t(b) * 2 * a.S;
+    const uint16_t* ssl = tsl + a.S;
+    const uint4* t4 = reinterpret_cast<const uint4*>(tsl);
+    const uint4* s4 = reinterpret_cast<const uint4*>(ssl);
+    const int64_t lloc = int64_t(a.labels[row]) - v0;  // the label's index within the slice
 
-    // ---- pass 1: HBM -> shared memory; whole-vocabulary statistics --------
-    Online ot = online_empty(), os = online_empty();
-    float se = 0.0f, xl = 0.0f;
-    for (int v = tid; v < nvec; v += 2 * kThr) {
-      const bool two = v + kThr < nvec;
-      const uint4 tw0 = ld_stream16(trow + 8 * v), sw0 = ld_stream16(srow + 8 * v);
-      uint4 tw1 = make_uint4(0, 0, 0, 0), sw1 = tw1;
-      if (two) {
-        tw1 = ld_stream16(trow + 8 * (v + kThr));
-        sw1 = ld_stream16(srow + 8 * (v + kThr));
+    // ---- pass 1: whole-vocabulary statistics (teacher; student unless TOPK) --
+    float tmax = -INFINITY, smax = -INFINITY;
+    for (int v = tid; v < nvec; v += kThr) {
+      const uint4 w = t4[v];
+      const float vm = vmax8(w);
+      tmax = fmaxf(tmax, vm);
+      if (TOPK) {
+        const uint32_t kb = key_of_f(vm) >> 4;
+        vbin[v] = uint16_t(kb);
+        atomicAdd(&vhist[kb], 1u);
+      } else {
+        smax = fmaxf(smax, vmax8(s4[v]));
       }
+    }
+    const float mt = tmax * ks, ms = smax * ks;  // maxima of the scaled values (ks > 0)
+    f2 zt = 0, zs = 0, bb = 0, se2 = 0;
+    {
+      const f2 KS = mk2(ks, ks), NMT = mk2(-mt, -mt), NMS = mk2(-ms, -ms);
+      for (int v = tid; v < nvec; v += kThr) {
+        const uint4 w = t4[v];
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (!TOPK) x = s4[v];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u == 1 && !two) break;
-        const int vv = v + u * kThr;
-        const uint4 tw = u ? tw1 : tw0, sw = u ? sw1 : sw0;
-        *reinterpret_cast<uint4*>(tsl + 8 * vv) = tw;
-        *reinterpret_cast<uint4*>(ssl + 8 * vv) = sw;
-        const uint32_t tv[4] = {tw.x, tw.y, tw.z, tw.w}, sv[4] = {sw.x, sw.y, sw.z, sw.w};
-        float xt[8], xs[8], tm = -INFINITY, sm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          xt[j] = __fmul_rn(bf16f(tv[j >> 1], j & 1), ks);
-          xs[j] = __fmul_rn(bf16f(sv[j >> 1], j & 1), ks);
-          tm = fmaxf(tm, xt[j]);
-          sm = fmaxf(sm, xs[j]);
-        }
-        {
-          const float m = fmaxf(ot.m, tm);
-          float z = __fmul_rn(ot.z, ex2(ot.m - m));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) z = __fadd_rn(z, ex2(xt[j] - m));
-          ot = Online{m, z, 0.0f};
-        }
-        if (!TOPK) {
-          const float m = fmaxf(os.m, sm);
-          const float f = ex2(os.m - m);
-          float z = __fmul_rn(os.z, f), b = __fmul_rn(os.b, f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float e = ex2(xs[j] - m);
-            z = __fadd_rn(z, e);
-            if (need_b) {  // sum of 2^(x_s - m) (x_s - x_t), the difference formed exactly first
-              const float dx = __fmul_rn(__fsub_rn(bf16f(sv[j >> 1], j & 1), bf16f(tv[j >> 1], j & 1)), ks);
-              b = __fmaf_rn(e, dx, b);
-            }
-          }
-          os = Online{m, z, b};
-          if (mse) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float d = __fsub_rn(bf16f(sv[j >> 1], j & 1), bf16f(tv[j >> 1], j & 1));
-              se = __fmaf_rn(d, d, se);
+        for (int i = 0; i < 4; ++i) {
+          const f2 t2 = bf2(word(w, i));
+          zt = add2(zt, ex2x2(fma2(t2, KS, NMT)));
+          if (!TOPK) {
+            const f2 s2 = bf2(word(x, i));
+            const f2 es = ex2x2(fma2(s2, KS, NMS));
+            zs = add2(zs, es);
+            if (RGRAD) bb = fma2(es, sub2(s2, t2), bb);
+            if (MSE) {
+              const f2 d = sub2(s2, t2);
+              se2 = fma2(d, d, se2);
             }
           }
         }
-        if (TOPK) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) atomicAdd(&hist1[okey(j & 1 ? tv[j >> 1] >> 16 : tv[j >> 1]) >> 4], 1u);
-        }
-        if (lloc >= 8 * vv && lloc < 8 * vv + 8) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (lloc == 8 * vv + j) xl = xt[j];
-        }
       }
     }
-    block_online2(ot, os, sh);
-    {
-      float v2[2] = {se, xl};
-      block_sum<2>(v2, sh);
-      se = v2[0];
-      xl = v2[1];
-    }
-    Online T_ = online_empty(), S_ = online_empty();
-    float SE = 0.0f, XL = 0.0f;
-    {
-      const float mine[8] = {ot.m, ot.z, ot.b, os.m, os.z, os.b, se, xl};
-      float all[kCl][8];
-      cluster_exchange<8>(mine, all, sh, par);
-#pragma unroll
-      for (int r = 0; r < kCl; ++r) {
-        T_ = online_merge(T_, Online{all[r][0], all[r][1], all[r][2]});
-        S_ = online_merge(S_, Online{all[r][3], all[r][4], all[r][5]});
-        SE = __fadd_rn(SE, all[r][6]);
-        XL = __fadd_rn(XL, all[r][7]);
-      }
-    }
+    const Online ot{mt, __fadd_rn(lo2(zt), hi2(zt)), 0.0f};
+    const Online os{ms, __fadd_rn(lo2(zs), hi2(zs)), __fmul_rn(__fadd_rn(lo2(bb), hi2(bb)), ks)};
+    const float se = __fadd_rn(lo2(se2), hi2(se2));
+    const float xl = (tid == 0 && lloc >= 0 && lloc < n64)
+                         ? __fmul_rn(__uint_as_float(uint32_t(tsl[lloc]) << 16), ks)
+                         : 0.0f;
+    const int kx = (TOPK && tmax > -INFINITY) ? int(key_of_f(tmax)) : 0;
+    const Rec R1 = cluster_rec<true>(block_rec<true>(Rec{ot, os, se, xl, kx}, sh), sh, par);
+    const Online T_ = R1.t, S_ = R1.s;
+    const float SE = R1.u, XL = R1.v;
+    const int kmax = R1.k;
     // conf: the whole-vocabulary teacher probability of the label
     const float conf = ex2(XL - (T_.m + log2f(T_.z)));
 
-    // ---- top-K support: threshold key, ties by index ------------------------
+    // ---- top-K support: threshold key, ties by index ----------------------
     uint32_t tkey = 0;
-    int idx_lim = -1;
+    int idx_lim = -1, tbin = 0;
     if (TOPK) {
-      // thread tid owns bins [8 g, 8 g + 8) with g = kThr - 1 - tid, so the
-      // scan over threads runs from the largest keys down
-      const int g = kThr - 1 - tid;
-      uint32_t hb[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-      for (int r = 0; r < kCl; ++r) {
-        const uint32_t base = remote_addr(hist1 + 8 * g, r);
-        const uint4 p = ld_remote_v4(base), q = ld_remote_v4(base + 16);
-        hb[0] += p.x; hb[1] += p.y; hb[2] += p.z; hb[3] += p.w;
-        hb[4] += q.x; hb[5] += q.y; hb[6] += q.z; hb[7] += q.w;
-      }
-      int c = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) c += int(hb[j]);
-      int total;
-      const int incl = block_scan(c, total, sh);
-      if (incl - c < a.K && incl >= a.K) {
-        int cum = incl - c;
-        for (int j = 7; j >= 0; --j) {
-          if (cum + int(hb[j]) >= a.K) {
-            sh->sel[0] = 8 * g + j;
-            sh->sel[1] = a.K - cum;
-            break;
-          }
-          cum += int(hb[j]);
-        }
-      }
-      __syncthreads();
-      const uint32_t bstar = uint32_t(sh->sel[0]);
-      const int need = sh->sel[1];
+      const int top = kmax >> 4;
+      int b0 = 0, above = 0;
+      if (!find_from_top(vhist, top, a.K, b0, above, sh)) b0 = 0;
+      // elements at or above the bound: 12-bit histogram
       for (int v = tid; v < nvec; v += kThr) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tsl + 8 * v);
-        const uint32_t tw[4] = {w.x, w.y, w.z, w.w};
+        if (int(vbin[v]) < b0) continue;
+        const uint4 w = t4[v];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint32_t k = okey(j & 1 ? tw[j >> 1] >> 16 : tw[j >> 1]);
-          if ((k >> 4) == bstar) atomicAdd(&sh->hist2[k & 15u], 1u);
+          const uint32_t k = key_of(w, j);
+          if (int(k >> 4) >= b0) atomicAdd(&hist1[k >> 4], 1u);
         }
       }
       __syncthreads();
       cluster_sync();
-      if (tid < kCl * 16) sh->h2all[tid >> 4][tid & 15] = ld_remote_u32(remote_addr(&sh->hist2[tid & 15], tid >> 4));
+      int bstar = 0;
+      find_from_top(hist1, top, a.K, bstar, above, sh);  // holds at least K
+      const int need = a.K - above;
+      for (int v = tid; v < nvec; v += kThr) {
+        if (int(vbin[v]) < bstar) continue;
+        const uint4 w = t4[v];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t k = key_of(w, j);
+          if (int(k >> 4) == bstar) atomicAdd(&sh->hist2[k & 15u], 1u);
+        }
+      }
+      __syncthreads();
+      cluster_sync();
+      if (tid < kCl * 16)
+        sh->h2all[tid >> 4][tid & 15] = ld_remote_u32(remote_addr(&sh->hist2[tid & 15], tid >> 4));
       __syncthreads();
       if (tid == 0) {
         int cum = 0, l = 15;
@@ -497,13 +629,14 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
         const int eq = int(sh->h2all[rank][l]);
         int take = q - before;
         take = take < 0 ? 0 : (take > eq ? eq : take);
-        sh->sel[2] = int((bstar << 4) | uint32_t(l));
+        sh->sel[2] = int((uint32_t(bstar) << 4) | uint32_t(l));
         sh->sel[3] = take;
         sh->sel[4] = eq;
         sh->sel[5] = -1;
       }
       __syncthreads();
       tkey = uint32_t(sh->sel[2]);
+      tbin = int(tkey >> 4);
       const int take = sh->sel[3], eq = sh->sel[4];
       if (take == eq) {
         idx_lim = 8 * nvec;
@@ -525,35 +658,24 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     int sel_before = 0;
     if (TOPK) {
       Online ut = online_empty(), us = online_empty();
-      float cnt = 0.0f;
+      int cnt = 0;
       for (int v = tid; v < nvec; v += kThr) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tsl + 8 * v);
-        const uint4 x = *reinterpret_cast<const uint4*>(ssl + 8 * v);
-        const uint32_t tw[4] = {w.x, w.y, w.z, w.w}, sw[4] = {x.x, x.y, x.z, x.w};
+        if (int(vbin[v]) < tbin) continue;
+        const uint4 w = t4[v], x = s4[v];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (!selected(8 * v + j, okey(j & 1 ? tw[j >> 1] >> 16 : tw[j >> 1]))) continue;
-          const float t = bf16f(tw[j >> 1], j & 1), s = bf16f(sw[j >> 1], j & 1);
-          const float xt = __fmul_rn(t, ks), xs = __fmul_rn(s, ks);
-          ut = online_merge(ut, Online{xt, 1.0f, 0.0f});
-          const float dx = __fmul_rn(__fsub_rn(s, t), ks);
-          us = online_merge(us, Online{xs, 1.0f, dx});
-          cnt += 1.0f;
+          if (!selected(8 * v + j, key_of(w, j))) continue;
+          const uint32_t tw = word(w, j >> 1), sw = word(x, j >> 1);
+          const float t = __uint_as_float(j & 1 ? tw & 0xFFFF0000u : tw << 16);
+          const float s = __uint_as_float(j & 1 ? sw & 0xFFFF0000u : sw << 16);
+          ut = online_merge(ut, Online{__fmul_rn(t, ks), 1.0f, 0.0f});
+          us = online_merge(us, Online{__fmul_rn(s, ks), 1.0f, __fmul_rn(__fsub_rn(s, t), ks)});
+          ++cnt;
         }
       }
-      block_online2(ut, us, sh);
-      float c1[1] = {cnt};
-      block_sum<1>(c1, sh);
-      const float mine[8] = {ut.m, ut.z, ut.b, us.m, us.z, us.b, c1[0], 0.0f};
-      float all[kCl][8];
-      cluster_exchange<8>(mine, all, sh, par);
-      Online UT = online_empty(), US = online_empty();
-#pragma unroll
-      for (int r = 0; r < kCl; ++r) {
-        UT = online_merge(UT, Online{all[r][0], all[r][1], all[r][2]});
-        US = online_merge(US, Online{all[r][3], all[r][4], all[r][5]});
-        if (uint32_t(r) < rank) sel_before += int(all[r][6]);
-      }
+      const Rec RS = cluster_rec<false>(block_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}, sh), sh, par,
+                                        &sel_before);
+      const Online UT = RS.t, US = RS.s;
       lse_t = UT.m + log2f(UT.z);
       lse_s = US.m + log2f(US.z);
       rkl0 = kLn2 * (US.b / US.z - (lse_s - lse_t));
@@ -563,56 +685,73 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
       rkl0 = kLn2 * (S_.b / S_.z - (lse_s - lse_t));
     }
 
-    // ---- pass 2 (shared memory): loss terms and the gradient -----------------
+    // ---- pass 2: loss terms and the gradient ---------------------------------
     const float dl = lse_t - lse_s;
     const float wf = a.type == AQFQ_KD_KL ? 1.0f : a.type == AQFQ_KD_RKL ? 0.0f : 1.0f - conf;
     const float wr = a.type == AQFQ_KD_KL ? 0.0f : a.type == AQFQ_KD_RKL ? 1.0f : conf;
-    float fs = 0.0f, rs = 0.0f;
+    const f2 KS = mk2(ks, ks), NLT = mk2(-lse_t, -lse_t), NLS = mk2(-lse_s, -lse_s);
+    const float kl = ks * kLn2, ndl = -dl * kLn2;
+    const f2 KL2 = mk2(kl, kl), NDL = mk2(ndl, ndl);
+    const f2 WF = mk2(gsc * wf, gsc * wf), NWR = mk2(-gsc * wr, -gsc * wr), RK = mk2(rkl0, rkl0);
+    const f2 GM = mk2(gsc, gsc);
+    f2 fs2 = 0, rs2 = 0;
     for (int v = tid; v < nvec; v += kThr) {
-      const uint4 w = *reinterpret_cast<const uint4*>(tsl + 8 * v);
-      const uint4 x = *reinterpret_cast<const uint4*>(ssl + 8 * v);
-      const uint32_t tw[4] = {w.x, w.y, w.z, w.w}, sw[4] = {x.x, x.y, x.z, x.w};
-      float g[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        g[j] = 0.0f;
-        if (TOPK && !selected(8 * v + j, okey(j & 1 ? tw[j >> 1] >> 16 : tw[j >> 1]))) continue;
-        const float t = bf16f(tw[j >> 1], j & 1), s = bf16f(sw[j >> 1], j & 1);
-        const float pt = ex2(__fmaf_rn(t, ks, -lse_t)), ps = ex2(__fmaf_rn(s, ks, -lse_s));
-        // log p_t - log p_s in nats
-        const float dn = kLn2 * (__fmul_rn(__fsub_rn(t, s), ks) - dl);
-        fs = __fadd_rn(fs, __fmaf_rn(pt, dn, ps - pt));
-        rs = __fadd_rn(rs, __fmaf_rn(-ps, dn, pt - ps));
-        if (drow)
-          g[j] = mse ? gsc * __fsub_rn(s, t) : gsc * (wf * (ps - pt) + wr * ps * (-dn - rkl0));
+      if (TOPK && int(vbin[v]) < tbin) {
+        if (drow) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
+        continue;
       }
-      if (drow)
-        st_stream16(drow + 8 * v, make_uint4(pack2(g[1], g[0]), pack2(g[3], g[2]), pack2(g[5], g[4]),
-                                             pack2(g[7], g[6])));
+      const uint4 w = t4[v], x = s4[v];
+      uint32_t out[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f2 t2 = bf2(word(w, i)), s2 = bf2(word(x, i));
+        f2 pt = ex2x2(fma2(t2, KS, NLT)), ps = ex2x2(fma2(s2, KS, NLS));
+        if (TOPK) {  // zero outside the support
+          const bool in0 = selected(8 * v + 2 * i, key_of(w, 2 * i));
+          const bool in1 = selected(8 * v + 2 * i + 1, key_of(w, 2 * i + 1));
+          pt = mk2(in0 ? lo2(pt) : 0.0f, in1 ? hi2(pt) : 0.0f);
+          ps = mk2(in0 ? lo2(ps) : 0.0f, in1 ? hi2(ps) : 0.0f);
+        }
+        const f2 dn = fma2(sub2(t2, s2), KL2, NDL);  // log p_t - log p_s in nats
+        const f2 diff = sub2(ps, pt);
+        fs2 = add2(fs2, fma2(pt, dn, diff));
+        rs2 = sub2(rs2, fma2(ps, dn, diff));
+        if (drow) {
+          f2 g;
+          if (MSE) g = mul2(sub2(s2, t2), GM);
+          else if (RGRAD) g = fma2(NWR, mul2(ps, add2(dn, RK)), mul2(WF, diff));
+          else g = mul2(WF, diff);
+          out[i] = pack2(g);
+        }
+      }
+      if (drow) st_stream16(drow + 8 * v, make_uint4(out[0], out[1], out[2], out[3]));
     }
+    // this slice's loss sums go to the workspace; the mean kernel adds the
+    // slices of each position in rank order (no exchange needed here)
     {
-      float v2[2] = {fs, rs};
-      block_sum<2>(v2, sh);
-      const float mine[2] = {v2[0], v2[1]};
-      float all[kCl][2];
-      cluster_exchange<2>(mine, all, sh, par);
-      float F = 0.0f, R = 0.0f;
+      float f = __fadd_rn(lo2(fs2), hi2(fs2)), r = __fadd_rn(lo2(rs2), hi2(rs2));
 #pragma unroll
-      for (int r = 0; r < kCl; ++r) {
-        F = __fadd_rn(F, all[r][0]);
-        R = __fadd_rn(R, all[r][1]);
+      for (int d = 16; d >= 1; d >>= 1) {
+        f = __fadd_rn(f, __shfl_xor_sync(0xFFFFFFFFu, f, d));
+        r = __fadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, d));
       }
-      F = a.tau2 * F;
-      R = a.tau2 * R;
-      if (rank == 0 && tid == 0) {
-        const float loss = a.type == AQFQ_KD_KL    ? F
-                           : a.type == AQFQ_KD_RKL ? R
-                           : a.type == AQFQ_KD_MSE ? SE / float(a.V)
-                                                   : conf * R + (1.0f - conf) * F;
-        a.tok[3 * row] = loss;
-        a.tok[3 * row + 1] = F;
-        a.tok[3 * row + 2] = R;
-        if (a.token_loss) a.token_loss[row] = loss;
+      if ((tid & 31) == 0) {
+        sh->red[tid >> 5][10] = f;
+        sh->red[tid >> 5][11] = r;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float F = 0.0f, R = 0.0f;
+        for (int k = 0; k < kWarps; ++k) {
+          F = __fadd_rn(F, sh->red[k][10]);
+          R = __fadd_rn(R, sh->red[k][11]);
+        }
+        a.part[(row * kCl + rank) * 2] = F;
+        a.part[(row * kCl + rank) * 2 + 1] = R;
+        if (rank == 0) {
+          a.rowx[2 * row] = conf;
+          a.rowx[2 * row + 1] = SE;
+        }
       }
     }
     if (TOPK && a.topk_idx) {  // the support in ascending vocabulary order
@@ -626,13 +765,29 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
           },
           sh);
     }
+    if (kNbuf == 1) {  // one buffer: refill it once every read of it is done
+      __syncthreads();
+      if (tid == 0) {
+        const int64_t after = next_valid(row + G);
+        if (after >= 0) {
+          sm100::fence_proxy_async_smem();
+          prefetch(after, 0);
+        }
+      }
+    }
+  }
+  // a copy whose wait timed out may still be landing: give it time before exit
+  if (tid == 0 && sh->err) {
+    sm100::mbar_wait(&sh->full[0], (uses[0] + 1u) & 1u);
+    sm100::mbar_wait(&sh->full[1], (uses[1] + 1u) & 1u);
+    atomicExch(&a.ws_head[1], 1);
   }
   // no CTA leaves while a peer may still read its shared memory
   cluster_sync();
 }
 
-// number of positions whose label lies in [0, V)
-__global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* out) {
+// number of positions whose label lies in [0, V); clears the error word
+__global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* head) {
   __shared__ int part[32];
   int c = 0;
   for (int64_t i = threadIdx.x; i < T; i += blockDim.x) c += (labels[i] >= 0 && labels[i] < V);
@@ -643,31 +798,57 @@ __global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int
   if (threadIdx.x == 0) {
     int s = 0;
     for (int k = 0; k < int(blockDim.x >> 5); ++k) s += part[k];
-    *out = s;
+    head[0] = s;
+    head[1] = 0;
   }
 }
 
-// losses[k] = sum over positions of tok[:, k] / number of valid positions
-// (ignored positions hold zeros); double accumulation, fixed order
-__global__ void kd_mean_kernel(const float* tok, const int32_t* nvalid, int64_t T, float* losses) {
-  __shared__ double part[32][3];
+// Per position: forward / reverse KL = tau^2 x the sum of the slices' sums
+// (rank order), the loss of the selected type, written to token_loss; then
+// losses[k] = the sums over the valid positions / their number (double
+// accumulation, fixed order); NaN if a copy wait of the loss kernel timed out.
+__global__ void kd_mean_kernel(const float* part, const float* rowx, const int32_t* labels,
+                               const int32_t* head, int64_t T, int64_t V, int type, float tau2,
+                               float* token_loss, float* losses) {
+  __shared__ double acc[32][3];
   double s[3] = {0.0, 0.0, 0.0};
-  for (int64_t i = threadIdx.x; i < T; i += blockDim.x)
-#pragma unroll
-    for (int k = 0; k < 3; ++k) s[k] += double(tok[3 * i + k]);
+  for (int64_t i = threadIdx.x; i < T; i += blockDim.x) {
+    const int32_t l = labels[i];
+    float loss = 0.0f;
+    if (l >= 0 && int64_t(l) < V) {
+      float F = 0.0f, R = 0.0f;
+      for (int r = 0; r < kCl; ++r) {
+        F = __fadd_rn(F, part[(i * kCl + r) * 2]);
+        R = __fadd_rn(R, part[(i * kCl + r) * 2 + 1]);
+      }
+      F = tau2 * F;
+      R = tau2 * R;
+      const float conf = rowx[2 * i];
+      loss = type == AQFQ_KD_MSE   ? rowx[2 * i + 1] / float(V)
+             : type == AQFQ_KD_KL  ? F
+             : type == AQFQ_KD_RKL ? R
+                                   : conf * R + (1.0f - conf) * F;
+      s[0] += double(loss);
+      s[1] += double(F);
+      s[2] += double(R);
+    }
+    if (token_loss) token_loss[i] = loss;
+  }
 #pragma unroll
   for (int k = 0; k < 3; ++k)
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) s[k] += __shfl_xor_sync(0xFFFFFFFFu, s[k], d);
   if ((threadIdx.x & 31) == 0)
 #pragma unroll
-    for (int k = 0; k < 3; ++k) part[threadIdx.x >> 5][k] = s[k];
+    for (int k = 0; k < 3; ++k) acc[threadIdx.x >> 5][k] = s[k];
   __syncthreads();
   if (threadIdx.x < 3) {
     double t = 0.0;
-    for (int w = 0; w < int(blockDim.x >> 5); ++w) t += part[w][threadIdx.x];
-    const int n = T > 0 ? *nvalid : 0;
-    losses[threadIdx.x] = n > 0 ? float(t / double(n)) : 0.0f;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) t += acc[w][threadIdx.x];
+    const int n = T > 0 ? head[0] : 0;
+    float r = n > 0 ? float(t / double(n)) : 0.0f;
+    if (T > 0 && head[1] != 0) r = __int_as_float(0x7FC00000);
+    losses[threadIdx.x] = r;
   }
 }
 
@@ -680,10 +861,14 @@ namespace {
 
 using namespace aqfq;
 
-constexpr size_t kWsHead = 256;  // workspace: int32 valid count, then tok [T, 3]
+// workspace: [0, 256) int32 valid count and error word; then part [T, kCl, 2]
+// and rowx [T, 2] floats, each starting on a 256-byte boundary
+constexpr size_t kWsHead = 256;
+size_t ws_part_bytes(int64_t T) { return (size_t(T) * kCl * 8 + 255) / 256 * 256; }
 
 size_t kd_smem_bytes(int32_t S, bool topk) {
-  return sizeof(KdShared) + (topk ? size_t(kHist1) * 4 : 0) + size_t(S) * 4;
+  const size_t vbin = topk ? size_t((S / 8 + 7) / 8 * 8) * 2 : 0;
+  return sizeof(KdShared) + (topk ? size_t(2 * kHist1) * 4 : 0) + vbin + size_t(S) * 4 * kNbuf;
 }
 
 int max_smem_optin() {
@@ -694,10 +879,12 @@ int max_smem_optin() {
   return v;
 }
 
-template <bool TOPK>
+template <bool TOPK, bool RGRAD, bool MSE>
 cudaError_t launch_kd(const KdArgs& a, size_t smem, cudaStream_t st) {
-  auto kern = kd_loss_kernel<TOPK>;
+  auto kern = kd_loss_kernel<TOPK, RGRAD, MSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -726,7 +913,7 @@ bool al(const void* p, uintptr_t b) { return (reinterpret_cast<uintptr_t>(p) & (
 
 extern "C" size_t aqfq_kd_workspace_bytes(int64_t T) {
   if (T < 0) return 0;
-  return kWsHead + ((size_t(T) * 12 + 255) / 256) * 256;
+  return kWsHead + ws_part_bytes(T) + (size_t(T) * 8 + 255) / 256 * 256;
 }
 
 extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void* teacher,
@@ -755,18 +942,19 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
   if (optin <= 0) return AQFQ_ERR_CUDA;
   if (smem > size_t(optin)) return AQFQ_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int32_t* nvalid = static_cast<int32_t*>(workspace);
-  float* tok = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead);
-  kd_count_kernel<<<1, 1024, 0, st>>>(labels, T, V, nvalid);
+  int32_t* head = static_cast<int32_t*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead);
+  float* rowx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead + ws_part_bytes(T));
+  kd_count_kernel<<<1, 1024, 0, st>>>(labels, T, V, head);
   if (cudaGetLastError() != cudaSuccess) return AQFQ_ERR_CUDA;
   if (T > 0) {
     KdArgs a;
     a.s = static_cast<const uint16_t*>(student);
     a.t = static_cast<const uint16_t*>(teacher);
     a.labels = labels;
-    a.nvalid = nvalid;
-    a.tok = tok;
-    a.token_loss = token_loss;
+    a.ws_head = head;
+    a.part = part;
+    a.rowx = rowx;
     a.ds = static_cast<uint16_t*>(dstudent);
     a.topk_idx = topk_idx;
     a.T = T;
@@ -778,9 +966,16 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
     a.tau2 = temperature * temperature;
     a.ks = kLog2e / temperature;
     a.grad_scale = grad_scale;
-    const cudaError_t e = use_topk ? launch_kd<true>(a, smem, st) : launch_kd<false>(a, smem, st);
+    const bool rgrad = dstudent && (kd_type == AQFQ_KD_RKL || kd_type == AQFQ_KD_CAKLD);
+    cudaError_t e;
+    if (kd_type == AQFQ_KD_MSE) e = launch_kd<false, false, true>(a, smem, st);
+    else if (use_topk) e = rgrad ? launch_kd<true, true, false>(a, smem, st)
+                                 : launch_kd<true, false, false>(a, smem, st);
+    else e = rgrad ? launch_kd<false, true, false>(a, smem, st)
+                   : launch_kd<false, false, false>(a, smem, st);
     if (e != cudaSuccess) return AQFQ_ERR_CUDA;
   }
-  kd_mean_kernel<<<1, 1024, 0, st>>>(tok, nvalid, T, losses);
+  kd_mean_kernel<<<1, 1024, 0, st>>>(part, rowx, labels, head, T, V, kd_type,
+                                     temperature * temperature, token_loss, losses);
   return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
 }

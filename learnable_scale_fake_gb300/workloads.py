@@ -15,6 +15,10 @@ step of its hot path with each call's algorithmic bytes:
   observer_fp8   per-head min/max of [65536,32,128] activations, per-head
                  scale, per-head E4M3 QDQ
   int8_channel   INT8 per-channel weight [256,512]: forward + scale gradient
+  kd_cakld       distillation loss of student vs teacher logits [4096, 151936]
+                 (Qwen3-sized vocabulary), cakld over the whole vocabulary,
+                 with the student-logit gradient
+  kd_topk        the same with forward KL over the teacher's top-1000 tokens
 
 Algorithmic bytes count what the call must move once: inputs read, outputs
 written (no codes: the steps do not request them).
@@ -360,6 +364,62 @@ def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8, experts=None):
     return wl
 
 
+def _kd(name, kd_type, topk, dev, seed=0, T=synth.KD_TOKENS, V=synth.KD_VOCAB):
+    """Distillation loss + student-logit gradient for T positions over a
+    V-token vocabulary (one aqfq_kd_loss call: count, loss and mean kernels).
+    Unfused reference path: the same loss in eager torch (fp32 log-softmax,
+    autograd for the gradient)."""
+    student, teacher, labels = synth.kd_logits(T, V, seed, dev)
+    losses = torch.empty(3, device=dev)
+    ds = torch.empty_like(student)
+    ws = torch.empty(aqfq.aqfq_kd_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    n = T * V
+    label = {aqfq.KD_CAKLD: "cakld", aqfq.KD_KL: "kl", aqfq.KD_RKL: "rkl", aqfq.KD_MSE: "mse"}[kd_type]
+    wl = Workload(name, f"distillation loss {label}{f' top-{topk}' if topk else ''}, logits [{T}, {V}]",
+                  {"workload": f"kd_{label}{f'_top{topk}' if topk else ''}_logits", "logits": [T, V],
+                   "loss": label, "topk": topk,
+                   "logits_recipe": "teacher N(0,4) + one favoured token +U(4,12); student = teacher "
+                                    "+ N(0,0.09); 10% ignored positions"})
+    wl.ops = [Op(f"kd_loss {label}", "kd_loss", n, 6 * n + 4 * T,
+                 lambda st: aqfq.aqfq_kd_loss(kd_type, student, teacher, labels, losses, ws, topk=topk,
+                                              dstudent=ds, stream=st), launches=3)]
+
+    def eager(st):
+        with torch.cuda.stream(st), torch.enable_grad():
+            sv = student.float().requires_grad_(True)
+            tv = teacher.float()
+            keep = (labels >= 0) & (labels < V)
+            idx = torch.nonzero(keep).squeeze(1)
+            a, b = tv[idx], sv[idx]
+            if topk:
+                sup = torch.topk(a, topk, dim=-1).indices
+                a, b = a.gather(1, sup), b.gather(1, sup)
+            lpt, lps = torch.log_softmax(a, -1), torch.log_softmax(b, -1)
+            fkl = (lpt.exp() * (lpt - lps)).sum(-1)
+            if kd_type == aqfq.KD_CAKLD:
+                rkl = (lps.exp() * (lps - lpt)).sum(-1)
+                conf = torch.softmax(tv[idx], -1).gather(1, labels[idx].long()[:, None]).squeeze(1)
+                loss = (conf * rkl + (1 - conf) * fkl).mean()
+            else:
+                loss = fkl.mean()
+            loss.backward()
+            ds.copy_(sv.grad)
+
+    wl.reference_ops = [Op("unfused: eager torch fp32 + autograd", "torch_eager", n, 6 * n + 4 * T, eager)]
+    wl.inputs.update({"student": student, "teacher": teacher, "labels": labels})
+    wl.outputs.update({"losses": losses, "dstudent": ds})
+    return wl
+
+
+def kd_cakld(dev, seed=0):
+    return _kd("kd_cakld", aqfq.KD_CAKLD, 0, dev, seed)
+
+
+def kd_topk(dev, seed=0):
+    return _kd("kd_topk", aqfq.KD_KL, 1000, dev, seed)
+
+
 BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
             "observer_fp8": observer_fp8, "int8_channel": int8_channel,
-            "head_fp8_learned": head_fp8_learned, "grouped_nvfp4_gemm": grouped_nvfp4_gemm}
+            "head_fp8_learned": head_fp8_learned, "grouped_nvfp4_gemm": grouped_nvfp4_gemm,
+            "kd_cakld": kd_cakld, "kd_topk": kd_topk}
