@@ -61,6 +61,7 @@ constexpr int kNbuf = AQFQ_KD_NBUF;   // slice buffers per CTA
 constexpr int kThr = 512;       // threads per CTA
 constexpr int kWarps = kThr / 32;
 constexpr int kHist1 = 4096;    // bins: the top 12 bits of the 16-bit teacher key
+constexpr int kHistWords = kHist1 / 2;  // two 16-bit counters per word (a slice has < 2^16 elements)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -83,7 +84,7 @@ struct KdArgs {
 
 struct __align__(16) KdShared {
   uint64_t full[2];         // mbarriers of the two slice buffers
-  float xbuf[2][12];        // exchange slots (alternating)
+  float xw[2][12];          // this CTA's reduction record (alternating exchange slots)
   float red[kWarps][12];    // block reductions
   int32_t ired[kWarps + 1];
   uint32_t hist2[16];       // low nibble of the keys in the threshold bin
@@ -239,6 +240,25 @@ __device__ __forceinline__ Online online_shfl(Online a, int d) {
                 __shfl_xor_sync(0xFFFFFFFFu, a.b, d)};
 }
 
+// Waits until the phase of `bar` with the given parity completes.  The thread
+// sleeps in mbarrier.try_wait (no polling loop issuing instructions); gives
+// up after about 2^31 clock cycles (~1 s) and returns false.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+}
+
 // A reduction record: online states of teacher and student, two sums and one
 // integer combined by max (KMAX) or by sum.
 struct Rec {
@@ -272,40 +292,32 @@ __device__ __forceinline__ Rec rec_load(const float* p) {
   return Rec{Online{p[0], p[1], p[2]}, Online{p[3], p[4], p[5]}, p[6], p[7], __float_as_int(p[8])};
 }
 
-// Block reduction of one record per thread; every thread gets the total.
-// Warps reduce by butterfly, then warp 0 merges the warps' records.
+// Cluster reduction of one record per warp (`wr`: the warp's total, the same in
+// every lane).  Warp 0 merges the warps' records into the CTA's record and
+// puts it in this CTA's exchange slot `par`; the cluster synchronises; warp 0
+// of every CTA reads the kCl CTA records (lane r from rank r), merges them in
+// a fixed order and broadcasts the total through shared memory, so all CTAs
+// hold bit-identical totals.  k_before (if not NULL) receives the sum of k
+// over the ranks below this one.  A slot is rewritten two exchanges later,
+// after a barrier that every CTA passes only once it has read the slot; the
+// warp records and the result are rewritten only after barriers that every
+// thread reaches after reading them.
 template <bool KMAX>
-__device__ __forceinline__ Rec block_rec(Rec a, KdShared* sh) {
+__device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par,
+                                           int* k_before = nullptr) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  a = warp_rec<KMAX>(a);
-  if (l == 0) rec_store(sh->red[w], a);
+  if (l == 0) rec_store(sh->red[w], wr);
   __syncthreads();
   if (w == 0) {
     Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
     x = warp_rec<KMAX>(x);
-    if (l == 0) rec_store(sh->res, x);
+    if (l == 0) rec_store(sh->xw[par], x);
   }
-  __syncthreads();
-  return rec_load(sh->res);
-}
-
-// Cluster reduction of one record per CTA (thread 0's `mine`): the record goes
-// to this CTA's exchange slot `par`, the cluster synchronises, warp 0 reads
-// the kCl records (lane r from rank r) and merges them by butterfly, the same
-// way in every CTA, so all CTAs hold bit-identical totals.  k_before (if not
-// NULL) receives the sum of k over the ranks below this one.  A slot is
-// rewritten two exchanges later, after a barrier that every CTA passes only
-// once it has read the slot.
-template <bool KMAX>
-__device__ __forceinline__ Rec cluster_rec(const Rec& mine, KdShared* sh, int& par,
-                                           int* k_before = nullptr) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (threadIdx.x == 0) rec_store(sh->xbuf[par], mine);
   cluster_sync();
   if (w == 0) {
     Rec x = rec_empty();
     if (l < kCl) {
-      const uint32_t base = remote_addr(&sh->xbuf[par][0], uint32_t(l));
+      const uint32_t base = remote_addr(&sh->xw[par][0], uint32_t(l));
       float v[9];
 #pragma unroll
       for (int i = 0; i < 9; ++i) v[i] = ld_remote_f32(base + 4u * i);
@@ -326,7 +338,6 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& mine, KdShared* sh, int& p
   __syncthreads();
   const Rec r = rec_load(sh->res);
   if (k_before) *k_before = __float_as_int(sh->res[9]);
-  __syncthreads();
   par ^= 1;
   return r;
 }
@@ -353,7 +364,8 @@ __device__ __forceinline__ int block_scan(int v, int& total, KdShared* sh) {
 }
 
 // After a cluster barrier: walking down from bin `top`, the bin at which the
-// cluster-wide count of a 4096-bin histogram reaches K, and the count above
+// cluster-wide count of a 4096-bin histogram (16-bit counters, bin b in half
+// b & 1 of word b >> 1) reaches K, and the count above
 // that bin.  Returns false (bin 0, the whole count) when the histogram holds
 // fewer than K.  All threads call it.  Each step covers 32 bins: thread t
 // loads bin t / 16 of the step from rank t % 16 (one remote load each).
@@ -365,7 +377,9 @@ __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int
   int base = 0;
   for (int b0 = top; b0 >= 0; b0 -= 32) {
     const int b = b0 - j;
-    uint32_t c = (part && b >= 0) ? ld_remote_u32(remote_addr(hist + b, r)) : 0u;
+    uint32_t c = (part && b >= 0)
+                     ? (ld_remote_u32(remote_addr(hist + (b >> 1), r)) >> ((b & 1) * 16)) & 0xFFFFu
+                     : 0u;
 #pragma unroll
     for (int d = kCl / 2; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
     if (part && r == 0) sh->bins[j] = c;
@@ -400,17 +414,20 @@ __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int
   return false;
 }
 
-// Visits the slice in index order and calls emit(local index, position) for
-// every element that satisfies pred(local index, key); the position counts
-// those elements from 0 in index order.  All threads call it.
+// Visits the vectors listed in cand[0..nc) (ascending vector indices) and calls
+// emit(local index, position) for every element that satisfies pred(local
+// index, key); the position counts those elements from 0 in index order.
+// All threads call it.
 template <class Pred, class Emit>
-__device__ __forceinline__ void ordered_scan(const uint16_t* tsl, int nvec, Pred pred, Emit emit,
-                                             KdShared* sh) {
+__device__ __forceinline__ void ordered_scan(const uint16_t* tsl, const uint16_t* cand, int nc,
+                                             Pred pred, Emit emit, KdShared* sh) {
   int base = 0;
-  for (int v00 = 0; v00 < nvec; v00 += kThr) {
-    const int v = v00 + int(threadIdx.x);
+  for (int p0 = 0; p0 < nc; p0 += kThr) {
+    const int p = p0 + int(threadIdx.x);
     uint32_t m8 = 0;
-    if (v < nvec) {
+    int v = 0;
+    if (p < nc) {
+      v = cand[p];
       const uint4 w = *reinterpret_cast<const uint4*>(tsl + 8 * v);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -437,12 +454,13 @@ template <bool TOPK, bool RGRAD, bool MSE>
 __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
   extern __shared__ __align__(16) uint8_t kd_smem[];
   KdShared* sh = reinterpret_cast<KdShared*>(kd_smem);
+  const int nvb = TOPK ? (a.S / 8 + 7) / 8 * 8 : 0;  // vector slots, padded to 16 bytes
   uint32_t* vhist = reinterpret_cast<uint32_t*>(kd_smem + sizeof(KdShared));  // vector-max bins
-  uint32_t* hist1 = vhist + (TOPK ? kHist1 : 0);                               // element bins
-  uint16_t* vbin = reinterpret_cast<uint16_t*>(hist1 + (TOPK ? kHist1 : 0));   // bin of each vector max
-  const int vbin_n = TOPK ? (a.S / 8 + 7) / 8 * 8 : 0;
-  uint16_t* buf0 = vbin + vbin_n;  // two buffers of [teacher S | student S]
-  const int tid = threadIdx.x;
+  uint32_t* hist1 = vhist + (TOPK ? kHistWords : 0);                           // element bins
+  uint16_t* vbin = reinterpret_cast<uint16_t*>(hist1 + (TOPK ? kHistWords : 0));  // bin of each vector max
+  uint16_t* cand = vbin + nvb;                                                 // candidate vectors
+  uint16_t* buf0 = cand + nvb;  // kNbuf buffers of [teacher S | student S]
+  const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const int64_t v0 = int64_t(rank) * a.S;  // first vocabulary index of this slice
   int64_t n64 = a.V - v0;
@@ -462,6 +480,10 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     sm100::mbar_init(&sh->full[1], 1);
     sh->err = 0;
     sm100::fence_barrier_init();
+  }
+  if (TOPK) {
+    for (int i = tid; i < 2 * kHistWords; i += kThr) vhist[i] = 0;
+    if (tid < 16) sh->hist2[tid] = 0;
   }
   __syncthreads();
 
@@ -496,30 +518,24 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     if (!is_valid(row)) {  // the same decision in every CTA of the cluster: no exchange
       if (drow)
         for (int v = tid; v < nvec; v += kThr) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
-      if (rank == 0) {
-        if (TOPK && a.topk_idx)
-          for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
-      }
+      if (TOPK && rank == 0 && a.topk_idx)
+        for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
       continue;
     }
     const int b = kNbuf == 2 ? (it & 1) : 0;
     ++it;
-    // every read of the other buffer (the previous position) is done: refill it
-    __syncthreads();
-    if (kNbuf == 2 && tid == 0) {
-      const int64_t after = next_valid(row + G);
-      if (after >= 0) {
-        sm100::fence_proxy_async_smem();
-        prefetch(after, b ^ 1);
+    if (kNbuf == 2) {  // every read of the other buffer (the previous position) is done: refill it
+      __syncthreads();
+      if (tid == 0) {
+        const int64_t after = next_valid(row + G);
+        if (after >= 0) {
+          sm100::fence_proxy_async_smem();
+          prefetch(after, b ^ 1);
+        }
       }
     }
-    if (TOPK) {  // peers finished reading these before the last exchange of the previous row
-      for (int i = tid; i < 2 * kHist1; i += kThr) vhist[i] = 0;
-      if (tid < 16) sh->hist2[tid] = 0;
-    }
-    if (!sm100::mbar_wait(&sh->full[b], uses[b] & 1u)) atomicExch(&sh->err, 1);
+    if (!wait_phase(&sh->full[b], uses[b] & 1u)) atomicExch(&sh->err, 1);
     ++uses[b];
-    __syncthreads();
     const uint16_t* tsl = buf0 + size_t(b) * 2 * a.S;
     const uint16_t* ssl = tsl + a.S;
     const uint4* t4 = reinterpret_cast<const uint4*>(tsl);
@@ -527,27 +543,43 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     const int64_t lloc = int64_t(a.labels[row]) - v0;  // the label's index within the slice
 
     // ---- pass 1: whole-vocabulary statistics (teacher; student unless TOPK) --
-    float tmax = -INFINITY, smax = -INFINITY;
-    for (int v = tid; v < nvec; v += kThr) {
-      const uint4 w = t4[v];
-      const float vm = vmax8(w);
-      tmax = fmaxf(tmax, vm);
-      if (TOPK) {
-        const uint32_t kb = key_of_f(vm) >> 4;
-        vbin[v] = uint16_t(kb);
-        atomicAdd(&vhist[kb], 1u);
-      } else {
-        smax = fmaxf(smax, vmax8(s4[v]));
-      }
-    }
-    const float mt = tmax * ks, ms = smax * ks;  // maxima of the scaled values (ks > 0)
+    // One read of each vector: per-thread running maxima of the scaled values,
+    // the sums rescaled when a vector raises them; warps then merge by
+    // butterfly and the cluster merges the warps' records.
+    float tmax = -INFINITY, smax = -INFINITY;  // raw (BF16) maxima
+    float mt = -INFINITY, ms = -INFINITY;      // scaled maxima: the sums' reference
     f2 zt = 0, zs = 0, bb = 0, se2 = 0;
     {
-      const f2 KS = mk2(ks, ks), NMT = mk2(-mt, -mt), NMS = mk2(-ms, -ms);
+      const f2 KS = mk2(ks, ks);
       for (int v = tid; v < nvec; v += kThr) {
         const uint4 w = t4[v];
+        const float vt = vmax8(w);
+        if (TOPK) {
+          const uint32_t kb = key_of_f(vt) >> 4;
+          vbin[v] = uint16_t(kb);
+          atomicAdd(&vhist[kb >> 1], 1u << ((kb & 1u) * 16));
+        }
+        if (vt > tmax) {
+          tmax = vt;
+          const float m = __fmul_rn(vt, ks), f = ex2(mt - m);
+          zt = mul2(zt, mk2(f, f));
+          mt = m;
+        }
+        const f2 NMT = mk2(-mt, -mt);
         uint4 x = make_uint4(0, 0, 0, 0);
-        if (!TOPK) x = s4[v];
+        f2 NMS = 0;
+        if (!TOPK) {
+          x = s4[v];
+          const float vs = vmax8(x);
+          if (vs > smax) {
+            smax = vs;
+            const float m = __fmul_rn(vs, ks), f = ex2(ms - m);
+            zs = mul2(zs, mk2(f, f));
+            if (RGRAD) bb = mul2(bb, mk2(f, f));
+            ms = m;
+          }
+          NMS = mk2(-ms, -ms);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const f2 t2 = bf2(word(w, i));
@@ -556,23 +588,30 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
             const f2 s2 = bf2(word(x, i));
             const f2 es = ex2x2(fma2(s2, KS, NMS));
             zs = add2(zs, es);
-            if (RGRAD) bb = fma2(es, sub2(s2, t2), bb);
-            if (MSE) {
+            if (RGRAD || MSE) {
               const f2 d = sub2(s2, t2);
-              se2 = fma2(d, d, se2);
+              if (RGRAD) bb = fma2(es, d, bb);
+              if (MSE) se2 = fma2(d, d, se2);
             }
           }
         }
       }
     }
-    const Online ot{mt, __fadd_rn(lo2(zt), hi2(zt)), 0.0f};
-    const Online os{ms, __fadd_rn(lo2(zs), hi2(zs)), __fmul_rn(__fadd_rn(lo2(bb), hi2(bb)), ks)};
-    const float se = __fadd_rn(lo2(se2), hi2(se2));
-    const float xl = (tid == 0 && lloc >= 0 && lloc < n64)
-                         ? __fmul_rn(__uint_as_float(uint32_t(tsl[lloc]) << 16), ks)
-                         : 0.0f;
-    const int kx = (TOPK && tmax > -INFINITY) ? int(key_of_f(tmax)) : 0;
-    const Rec R1 = cluster_rec<true>(block_rec<true>(Rec{ot, os, se, xl, kx}, sh), sh, par);
+    // the label's scaled teacher value, from the thread whose vectors hold it
+    const bool owns_label = lloc >= 0 && lloc < n64 && int((lloc >> 3) % kThr) == tid;
+    const float xl = owns_label ? __fmul_rn(__uint_as_float(uint32_t(tsl[lloc]) << 16), ks) : 0.0f;
+    const Rec mine{Online{mt, __fadd_rn(lo2(zt), hi2(zt)), 0.0f},
+                   Online{ms, __fadd_rn(lo2(zs), hi2(zs)), __fmul_rn(__fadd_rn(lo2(bb), hi2(bb)), ks)},
+                   __fadd_rn(lo2(se2), hi2(se2)), 0.0f,
+                   (TOPK && tmax > -INFINITY) ? int(key_of_f(tmax)) : 0};
+    Rec wr = warp_rec<true>(mine);
+    {  // the label's value: one thread of one CTA holds it; the butterfly adds zeros
+      float x = xl;
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, d));
+      wr.v = x;
+    }
+    const Rec R1 = cluster_rec<true>(wr, sh, par);
     const Online T_ = R1.t, S_ = R1.s;
     const float SE = R1.u, XL = R1.v;
     const int kmax = R1.k;
@@ -581,19 +620,31 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
 
     // ---- top-K support: threshold key, ties by index ----------------------
     uint32_t tkey = 0;
-    int idx_lim = -1, tbin = 0;
+    int idx_lim = -1, tbin = 0, nc = 0;
     if (TOPK) {
       const int top = kmax >> 4;
       int b0 = 0, above = 0;
       if (!find_from_top(vhist, top, a.K, b0, above, sh)) b0 = 0;
+      {  // candidate vectors (maximum at or above the bound), ascending: a
+         // contiguous range of vectors per thread and one block scan
+        const int per = (nvec + kThr - 1) / kThr, v0t = tid * per;
+        const int v1t = min(nvec, v0t + per);
+        int c = 0;
+        for (int v = v0t; v < v1t; ++v) c += int(vbin[v]) >= b0;
+        int total;
+        int pos = block_scan(c, total, sh) - c;
+        for (int v = v0t; v < v1t; ++v)
+          if (int(vbin[v]) >= b0) cand[pos++] = uint16_t(v);
+        nc = total;
+        __syncthreads();
+      }
       // elements at or above the bound: 12-bit histogram
-      for (int v = tid; v < nvec; v += kThr) {
-        if (int(vbin[v]) < b0) continue;
-        const uint4 w = t4[v];
+      for (int p = tid; p < nc; p += kThr) {
+        const uint4 w = t4[cand[p]];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t k = key_of(w, j);
-          if (int(k >> 4) >= b0) atomicAdd(&hist1[k >> 4], 1u);
+          if (int(k >> 4) >= b0) atomicAdd(&hist1[k >> 5], 1u << (((k >> 4) & 1u) * 16));
         }
       }
       __syncthreads();
@@ -601,7 +652,8 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
       int bstar = 0;
       find_from_top(hist1, top, a.K, bstar, above, sh);  // holds at least K
       const int need = a.K - above;
-      for (int v = tid; v < nvec; v += kThr) {
+      for (int p = tid; p < nc; p += kThr) {
+        const int v = cand[p];
         if (int(vbin[v]) < bstar) continue;
         const uint4 w = t4[v];
 #pragma unroll
@@ -642,7 +694,7 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
         idx_lim = 8 * nvec;
       } else if (take > 0) {  // the take-th equal element in index order
         ordered_scan(
-            tsl, nvec, [&](int, uint32_t k) { return k == tkey; },
+            tsl, cand, nc, [&](int, uint32_t k) { return k == tkey; },
             [&](int i, int pos) {
               if (pos + 1 == take) sh->sel[5] = i;
             },
@@ -659,7 +711,8 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     if (TOPK) {
       Online ut = online_empty(), us = online_empty();
       int cnt = 0;
-      for (int v = tid; v < nvec; v += kThr) {
+      for (int p = tid; p < nc; p += kThr) {
+        const int v = cand[p];
         if (int(vbin[v]) < tbin) continue;
         const uint4 w = t4[v], x = s4[v];
 #pragma unroll
@@ -673,12 +726,11 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
           ++cnt;
         }
       }
-      const Rec RS = cluster_rec<false>(block_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}, sh), sh, par,
+      const Rec RS = cluster_rec<false>(warp_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}), sh, par,
                                         &sel_before);
-      const Online UT = RS.t, US = RS.s;
-      lse_t = UT.m + log2f(UT.z);
-      lse_s = US.m + log2f(US.z);
-      rkl0 = kLn2 * (US.b / US.z - (lse_s - lse_t));
+      lse_t = RS.t.m + log2f(RS.t.z);
+      lse_s = RS.s.m + log2f(RS.s.z);
+      rkl0 = kLn2 * (RS.s.b / RS.s.z - (lse_s - lse_t));
     } else {
       lse_t = T_.m + log2f(T_.z);
       lse_s = S_.m + log2f(S_.z);
@@ -688,44 +740,59 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     // ---- pass 2: loss terms and the gradient ---------------------------------
     const float dl = lse_t - lse_s;
     const float wf = a.type == AQFQ_KD_KL ? 1.0f : a.type == AQFQ_KD_RKL ? 0.0f : 1.0f - conf;
-    const float wr = a.type == AQFQ_KD_KL ? 0.0f : a.type == AQFQ_KD_RKL ? 1.0f : conf;
+    const float wr2 = a.type == AQFQ_KD_KL ? 0.0f : a.type == AQFQ_KD_RKL ? 1.0f : conf;
     const f2 KS = mk2(ks, ks), NLT = mk2(-lse_t, -lse_t), NLS = mk2(-lse_s, -lse_s);
     const float kl = ks * kLn2, ndl = -dl * kLn2;
     const f2 KL2 = mk2(kl, kl), NDL = mk2(ndl, ndl);
-    const f2 WF = mk2(gsc * wf, gsc * wf), NWR = mk2(-gsc * wr, -gsc * wr), RK = mk2(rkl0, rkl0);
-    const f2 GM = mk2(gsc, gsc);
-    f2 fs2 = 0, rs2 = 0;
-    for (int v = tid; v < nvec; v += kThr) {
-      if (TOPK && int(vbin[v]) < tbin) {
-        if (drow) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
-        continue;
-      }
+    // gradient: gsc (wf (p_s - p_t) - wr p_s (d + rkl)) = p_s (c - gsc wr d) - gsc wf p_t
+    const f2 WF = mk2(gsc * wf, gsc * wf), NWF = mk2(-gsc * wf, -gsc * wf);
+    const f2 NWR = mk2(-gsc * wr2, -gsc * wr2);
+    const float c = gsc * wf - gsc * wr2 * rkl0;
+    const f2 C2 = mk2(c, c), NGM = mk2(-gsc, -gsc);
+    // the reverse sum: (p_t d - p_t + p_s) + (-p_s d - p_s + p_t) = -(p_s - p_t) d,
+    // so it is formed from q = sum (p_s - p_t) d and the forward sum
+    f2 fs2 = 0, q2 = 0;
+    auto pass2_vector = [&](int v, bool masked) {
       const uint4 w = t4[v], x = s4[v];
       uint32_t out[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const f2 t2 = bf2(word(w, i)), s2 = bf2(word(x, i));
         f2 pt = ex2x2(fma2(t2, KS, NLT)), ps = ex2x2(fma2(s2, KS, NLS));
-        if (TOPK) {  // zero outside the support
+        if (masked) {  // zero outside the support
           const bool in0 = selected(8 * v + 2 * i, key_of(w, 2 * i));
           const bool in1 = selected(8 * v + 2 * i + 1, key_of(w, 2 * i + 1));
           pt = mk2(in0 ? lo2(pt) : 0.0f, in1 ? hi2(pt) : 0.0f);
           ps = mk2(in0 ? lo2(ps) : 0.0f, in1 ? hi2(ps) : 0.0f);
         }
-        const f2 dn = fma2(sub2(t2, s2), KL2, NDL);  // log p_t - log p_s in nats
+        const f2 d2 = sub2(t2, s2);
+        const f2 dn = fma2(d2, KL2, NDL);  // log p_t - log p_s in nats
         const f2 diff = sub2(ps, pt);
         fs2 = add2(fs2, fma2(pt, dn, diff));
-        rs2 = sub2(rs2, fma2(ps, dn, diff));
+        q2 = fma2(diff, dn, q2);
         if (drow) {
           f2 g;
-          if (MSE) g = mul2(sub2(s2, t2), GM);
-          else if (RGRAD) g = fma2(NWR, mul2(ps, add2(dn, RK)), mul2(WF, diff));
+          if (MSE) g = mul2(d2, NGM);
+          else if (RGRAD) g = fma2(ps, fma2(NWR, dn, C2), mul2(NWF, pt));
           else g = mul2(WF, diff);
           out[i] = pack2(g);
         }
       }
       if (drow) st_stream16(drow + 8 * v, make_uint4(out[0], out[1], out[2], out[3]));
+    };
+    if (TOPK) {  // zeros outside the support's vectors, then the candidates densely
+      if (drow)
+        for (int v = tid; v < nvec; v += kThr)
+          if (int(vbin[v]) < tbin) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
+      for (int p = tid; p < nc; p += kThr) {
+        const int v = cand[p];
+        if (int(vbin[v]) >= tbin) pass2_vector(v, true);
+      }
+    } else {
+      for (int v = tid; v < nvec; v += kThr) pass2_vector(v, false);
     }
+    const f2 rs2 = sub2(mk2(0.0f, 0.0f), add2(q2, fs2));
+
     // this slice's loss sums go to the workspace; the mean kernel adds the
     // slices of each position in rank order (no exchange needed here)
     {
@@ -735,23 +802,9 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
         f = __fadd_rn(f, __shfl_xor_sync(0xFFFFFFFFu, f, d));
         r = __fadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, d));
       }
-      if ((tid & 31) == 0) {
+      if (lane == 0) {
         sh->red[tid >> 5][10] = f;
         sh->red[tid >> 5][11] = r;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float F = 0.0f, R = 0.0f;
-        for (int k = 0; k < kWarps; ++k) {
-          F = __fadd_rn(F, sh->red[k][10]);
-          R = __fadd_rn(R, sh->red[k][11]);
-        }
-        a.part[(row * kCl + rank) * 2] = F;
-        a.part[(row * kCl + rank) * 2 + 1] = R;
-        if (rank == 0) {
-          a.rowx[2 * row] = conf;
-          a.rowx[2 * row + 1] = SE;
-        }
       }
     }
     if (TOPK && a.topk_idx) {  // the support in ascending vocabulary order
@@ -759,15 +812,26 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
       const int32_t vb = int32_t(v0);
       const int room = a.K - sel_before;  // a support larger than K is never written past the row
       ordered_scan(
-          tsl, nvec, selected,
+          tsl, cand, nc, selected,
           [&](int i, int pos) {
             if (pos < room) out[pos] = vb + i;
           },
           sh);
     }
-    if (kNbuf == 1) {  // one buffer: refill it once every read of it is done
-      __syncthreads();
-      if (tid == 0) {
+    __syncthreads();  // every read of this row's buffer and histograms is done
+    if (tid == 0) {
+      float F = 0.0f, R = 0.0f;
+      for (int k = 0; k < kWarps; ++k) {
+        F = __fadd_rn(F, sh->red[k][10]);
+        R = __fadd_rn(R, sh->red[k][11]);
+      }
+      a.part[(row * kCl + rank) * 2] = F;
+      a.part[(row * kCl + rank) * 2 + 1] = R;
+      if (rank == 0) {
+        a.rowx[2 * row] = conf;
+        a.rowx[2 * row + 1] = SE;
+      }
+      if (kNbuf == 1) {  // one buffer: refill it
         const int64_t after = next_valid(row + G);
         if (after >= 0) {
           sm100::fence_proxy_async_smem();
@@ -775,11 +839,16 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
         }
       }
     }
+    if (TOPK) {  // peers read these before the support-statistics exchange
+      for (int i = tid; i < 2 * kHistWords; i += kThr) vhist[i] = 0;
+      if (tid < 16) sh->hist2[tid] = 0;
+    }
+    __syncthreads();
   }
   // a copy whose wait timed out may still be landing: give it time before exit
   if (tid == 0 && sh->err) {
-    sm100::mbar_wait(&sh->full[0], (uses[0] + 1u) & 1u);
-    sm100::mbar_wait(&sh->full[1], (uses[1] + 1u) & 1u);
+    wait_phase(&sh->full[0], (uses[0] + 1u) & 1u);
+    wait_phase(&sh->full[1], (uses[1] + 1u) & 1u);
     atomicExch(&a.ws_head[1], 1);
   }
   // no CTA leaves while a peer may still read its shared memory
@@ -867,8 +936,8 @@ constexpr size_t kWsHead = 256;
 size_t ws_part_bytes(int64_t T) { return (size_t(T) * kCl * 8 + 255) / 256 * 256; }
 
 size_t kd_smem_bytes(int32_t S, bool topk) {
-  const size_t vbin = topk ? size_t((S / 8 + 7) / 8 * 8) * 2 : 0;
-  return sizeof(KdShared) + (topk ? size_t(2 * kHist1) * 4 : 0) + vbin + size_t(S) * 4 * kNbuf;
+  const size_t vbin = topk ? size_t((S / 8 + 7) / 8 * 8) * 4 : 0;  // vector bins + candidate list
+  return sizeof(KdShared) + (topk ? size_t(2 * kHistWords) * 4 : 0) + vbin + size_t(S) * 4 * kNbuf;
 }
 
 int max_smem_optin() {
@@ -885,6 +954,9 @@ cudaError_t launch_kd(const KdArgs& a, size_t smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  // all of the unified L1 / shared memory as shared memory: two CTAs per SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
