@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="grouped_nvfp4")
     ap.add_argument("--experts", type=int, default=None,
                     help="grouped_nvfp4 only: truncate the expert axis (small profiling case)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="kd_cakld / kd_topk only: number of positions (small profiling case)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     return ap.parse_args()
@@ -74,30 +76,31 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
-    """Hash of the CUDA sources: a stored ncu traffic figure is valid only for it."""
+def source_digest(files):
+    """Hash of the named CUDA sources (paths relative to the repository): a
+    stored ncu traffic figure is valid only for the sources it was taken on."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "learnable_scale_fake_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    for f in sorted(files):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def stored_traffic(op_name):
-    """DRAM bytes per launch of op `op_name` from the committed ncu summary, if
-    the summary was taken on the current sources; else None."""
+    """DRAM bytes per launch of op `op_name` from the committed ncu summary
+    (profiles/traffic.md), if it was taken on the current state of the sources
+    its row names; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
-    digest = source_digest()
     for line in open(p):
-        tok = line.strip().strip("|").split("|")
-        tok = [t.strip() for t in tok]
-        if len(tok) >= 3 and tok[0] == op_name and tok[2] == digest:
+        tok = [t.strip() for t in line.strip().strip("|").split("|")]
+        if len(tok) >= 4 and tok[0] == op_name:
+            files = [f.strip() for f in tok[3].split(",") if f.strip()]
             try:
-                return int(tok[1])
-            except ValueError:
+                if files and tok[2] == source_digest(files):
+                    return int(tok[1])
+            except (OSError, ValueError):
                 return None
     return None
 
@@ -399,6 +402,8 @@ def main():
 
     if args.experts is not None and args.workload in ("grouped_nvfp4", "grouped_nvfp4_gemm"):
         wl = workloads.BUILDERS[args.workload](device, experts=args.experts)
+    elif args.tokens is not None and args.workload in ("kd_cakld", "kd_topk"):
+        wl = workloads.BUILDERS[args.workload](device, tokens=args.tokens)
     else:
         wl = workloads.BUILDERS[args.workload](device)
     stream = torch.cuda.Stream(device)

@@ -380,7 +380,11 @@ def _kd(name, kd_type, topk, dev, seed=0, T=synth.KD_TOKENS, V=synth.KD_VOCAB):
                    "loss": label, "topk": topk,
                    "logits_recipe": "teacher N(0,4) + one favoured token +U(4,12); student = teacher "
                                     "+ N(0,0.09); 10% ignored positions"})
-    wl.ops = [Op(f"kd_loss {label}", "kd_loss", n, 6 * n + 4 * T,
+    # algorithmic bytes: both logit rows read and the gradient row written at
+    # each valid position; only the (zero) gradient row at an ignored one
+    n_valid = int(((labels >= 0) & (labels < V)).sum())
+    nbytes = 6 * n_valid * V + 2 * (T - n_valid) * V + 4 * T
+    wl.ops = [Op(f"kd_loss {label}", "kd_loss", n, nbytes,
                  lambda st: aqfq.aqfq_kd_loss(kd_type, student, teacher, labels, losses, ws, topk=topk,
                                               dstudent=ds, stream=st), launches=3)]
 
@@ -405,18 +409,18 @@ def _kd(name, kd_type, topk, dev, seed=0, T=synth.KD_TOKENS, V=synth.KD_VOCAB):
             loss.backward()
             ds.copy_(sv.grad)
 
-    wl.reference_ops = [Op("unfused: eager torch fp32 + autograd", "torch_eager", n, 6 * n + 4 * T, eager)]
+    wl.reference_ops = [Op("unfused: eager torch fp32 + autograd", "torch_eager", n, nbytes, eager)]
     wl.inputs.update({"student": student, "teacher": teacher, "labels": labels})
     wl.outputs.update({"losses": losses, "dstudent": ds})
     return wl
 
 
-def kd_cakld(dev, seed=0):
-    return _kd("kd_cakld", aqfq.KD_CAKLD, 0, dev, seed)
+def kd_cakld(dev, seed=0, tokens=synth.KD_TOKENS):
+    return _kd("kd_cakld", aqfq.KD_CAKLD, 0, dev, seed, T=tokens)
 
 
-def kd_topk(dev, seed=0):
-    return _kd("kd_topk", aqfq.KD_KL, 1000, dev, seed)
+def kd_topk(dev, seed=0, tokens=synth.KD_TOKENS):
+    return _kd("kd_topk", aqfq.KD_KL, 1000, dev, seed, T=tokens)
 
 
 BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,

@@ -154,3 +154,43 @@ def test_reproducible_bits():
     np.testing.assert_array_equal(a["ds_bits"], b["ds_bits"])
     np.testing.assert_array_equal(a["tok"], b["tok"])
     np.testing.assert_array_equal(a["losses"], b["losses"])
+
+
+@pytest.mark.parametrize("name", ["kd_cakld", "kd_topk"])
+def test_full_size_bench_workload(name):
+    """The bench workloads (4096 positions x 151936 vocabulary, the same call
+    and launch configuration): every position's loss and the means against
+    the oracle on all rows; the gradient and the top-K support on sampled rows."""
+    from learnable_scale_fake_gb300 import workloads
+
+    wl = workloads.BUILDERS[name](torch.device(DEV))
+    s, t, lab = wl.inputs["student"], wl.inputs["teacher"], wl.inputs["labels"]
+    T, V = s.shape
+    kt, topk = (O.KD_CAKLD, 0) if name == "kd_cakld" else (O.KD_KL, 1000)
+    tl = torch.empty(T, device=DEV)
+    idx = torch.empty((T, topk), dtype=torch.int32, device=DEV) if topk else None
+    wl.ops[0].run(torch.cuda.current_stream())  # the bench's call
+    ws = torch.empty(aqfq.aqfq_kd_workspace_bytes(T), dtype=torch.uint8, device=DEV)
+    losses = torch.empty(3, device=DEV)
+    aqfq.aqfq_kd_loss(kt, s, t, lab, losses, ws, topk=topk, token_loss=tl, topk_idx=idx)
+    torch.cuda.synchronize()
+    labn = lab.cpu().numpy()
+    valid = (labn >= 0) & (labn < V)
+    r = O.kd_loss(kt, bits(s), bits(t), labn, topk=topk, want_grad=False)
+    g_tok = tl.cpu().double().numpy()
+    tol = np.where(valid, 2.0 ** -20 * r["cond"][:, 0], 0)
+    assert np.all(np.abs(g_tok - r["tok"][:, 0]) <= tol)
+    n = valid.sum()
+    g_loss = losses.cpu().double().numpy()
+    for k in range(3):
+        assert abs(g_loss[k] - r["losses"][k]) <= 2.0 ** -20 * r["cond"][valid, 0].sum() / n
+    # the bench call's gradient on sampled rows (the oracle on those rows alone,
+    # its gradient scale set to the full problem's 1 / n_valid)
+    rows = np.array([0, 1, 2, 777, 2048, 3001, T - 2, T - 1])
+    sub = O.kd_loss(kt, bits(s[rows]), bits(t[rows]), labn[rows], topk=topk,
+                    grad_scale=float(((labn[rows] >= 0) & (labn[rows] < V)).sum()) / n)
+    gds = wl.outputs["dstudent"][rows].cpu().float().double().numpy()
+    ds_tol = 2.0 ** -8 * np.abs(sub["dstudent"]) + 2.0 ** -18 * sub["gmag"]
+    assert np.all(np.abs(gds - sub["dstudent"]) <= ds_tol)
+    if topk:
+        np.testing.assert_array_equal(idx[rows].cpu().numpy(), sub["topk_idx"])
