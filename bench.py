@@ -320,7 +320,7 @@ def reference_arm(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     import oracle
-    from learnable_scale_fake_gb300 import synth
+    from learnable_scale_fake_gb300 import synth, workloads
 
     gen = {"grouped_nvfp4": lambda: synth.cfg3("cpu", 0, experts=8), "nvfp4_wa": lambda: synth.cfg2("cpu"),
            "int4_fp8": lambda: synth.cfg4("cpu"), "int8_channel": lambda: synth.cfg1("cpu"),
@@ -350,7 +350,7 @@ def reference_arm(args):
         "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * ts / len(runs), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "sample": desc},
+        "data": "synthetic", "config": dict(workloads.CONFIGS[args.workload], sample=desc),
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,

@@ -168,15 +168,42 @@ class _ExpertSlice:
         return self._pairs(wl.outputs, hout, wl)
 
 
+# The configuration each workload reports (bench.py's "config"), at its
+# default size; builders start from these, so the reference arm can report
+# the same dictionary without building device tensors.
+CONFIGS = {
+    "grouped_nvfp4": {"workload": "grouped_nvfp4_moe_stacks", "gate_up": [128, 1536, 2048],
+                      "down": [128, 2048, 768],
+                      "format": "nvfp4 (e2m1, 16-elem blocks, e4m3 block scale, fp32 tensor scale)",
+                      "values": "student-t(4)*0.02, 0.05% outliers x20",
+                      "scale_init": "amax/6, amax/2688"},
+    "nvfp4_wa": {"workload": "nvfp4_weight_activation", "w": [4096, 4096], "a": [8192, 4096]},
+    "int4_fp8": {"workload": "int4_g128_stack_fp8_channel_dense", "stack": [128, 1536, 2048],
+                 "dense": [8192, 8192]},
+    "observer_fp8": {"workload": "per_head_observer_fp8", "act": [65536, 32, 128]},
+    "head_fp8_learned": {"workload": "per_head_learnable_fp8", "act": [65536, 32, 128]},
+    "int8_channel": {"workload": "int8_per_channel_weight", "w": [256, 512]},
+    "grouped_nvfp4_gemm": {"workload": "grouped_nvfp4_gemm_gate_up", "x": [65536, 2048],
+                           "w": [128, 1536, 2048],
+                           "routing": "multinomial, expert popularity exp(N(0,0.3^2))"},
+    "kd_cakld": {"workload": "kd_cakld_logits", "logits": [synth.KD_TOKENS, synth.KD_VOCAB],
+                 "loss": "cakld", "topk": 0},
+    "kd_topk": {"workload": "kd_kl_top1000_logits", "logits": [synth.KD_TOKENS, synth.KD_VOCAB],
+                "loss": "kl", "topk": 1000},
+}
+_KD_RECIPE = ("teacher N(0,4) + one favoured token +U(4,12); student = teacher + N(0,0.09); "
+              "10% ignored positions")
+for _k in ("kd_cakld", "kd_topk"):
+    CONFIGS[_k]["logits_recipe"] = _KD_RECIPE
+
+
 def grouped_nvfp4(dev, seed=0, experts=None):
     d = synth.cfg3(dev, seed, experts)
     wl = Workload("grouped_nvfp4",
                   "grouped NVFP4 MoE expert stacks gate_up [E,1536,2048] + down [E,2048,768], "
                   "vectorised QDQ fwd + per-block scale grad",
-                  {"workload": "grouped_nvfp4_moe_stacks",
-                   "gate_up": list(d["gate_up"].shape), "down": list(d["down"].shape),
-                   "format": "nvfp4 (e2m1, 16-elem blocks, e4m3 block scale, fp32 tensor scale)",
-                   "values": "student-t(4)*0.02, 0.05% outliers x20", "scale_init": "amax/6, amax/2688"})
+                  dict(CONFIGS["grouped_nvfp4"], gate_up=list(d["gate_up"].shape),
+                       down=list(d["down"].shape)))
     for nm in ("gate_up", "down"):
         _nvfp4_stack(nm, d[nm], d[f"dy_{nm}"], dev, wl.ops, wl.inputs, wl.outputs)
     # order: both forwards, then both gradients (forward pass, then backward pass)
@@ -192,7 +219,7 @@ def grouped_nvfp4(dev, seed=0, experts=None):
 def nvfp4_wa(dev, seed=0):
     d = synth.cfg2(dev, seed)
     wl = Workload("nvfp4_wa", "NVFP4 weight [4096,4096] + activations [8192,4096]",
-                  {"workload": "nvfp4_weight_activation", "w": [4096, 4096], "a": [8192, 4096]})
+                  dict(CONFIGS["nvfp4_wa"]))
     w = d["w"].unsqueeze(0)
     _nvfp4_stack("w", w, d["dy_w"].unsqueeze(0), dev, wl.ops, wl.inputs, wl.outputs, grouped=False)
     a, dya = d["a"].unsqueeze(0), d["dy_a"].unsqueeze(0)
@@ -217,7 +244,7 @@ def nvfp4_wa(dev, seed=0):
 def int4_fp8(dev, seed=0):
     d = synth.cfg4(dev, seed)
     wl = Workload("int4_fp8", "INT4 g128 stack [128,1536,2048] + FP8 per-channel [8192,8192]",
-                  {"workload": "int4_g128_stack_fp8_channel_dense"})
+                  dict(CONFIGS["int4_fp8"]))
     st4 = Q(aqfq.INT4, aqfq.PER_GROUP, group=128, qmin=-8, qmax=7)
     x4, dy4 = d["stack"], d["dy_stack"]
     s4 = torch.empty(x4.numel() // 128, device=dev)
@@ -251,7 +278,7 @@ def observer_fp8(dev, seed=0):
     x = d["act"]
     T, H, D = x.shape
     wl = Workload("observer_fp8", "per-head observer + E4M3 QDQ on [65536,32,128]",
-                  {"workload": "per_head_observer_fp8", "act": [T, H, D]})
+                  dict(CONFIGS["observer_fp8"], act=[T, H, D]))
     mn, mx, s = (torch.empty(H, device=dev) for _ in range(3))
     y = torch.empty_like(x)
     sp = Q(aqfq.FP8_E4M3, aqfq.PER_HEAD)
@@ -285,7 +312,7 @@ def head_fp8_learned(dev, seed=0):
                      dtype=torch.float64, device=dev)
     n = x.numel()
     wl = Workload("head_fp8_learned", "per-head learnable FP8 QDQ on [65536,32,128]: fwd + scale grad + dx",
-                  {"workload": "per_head_learnable_fp8", "act": [T, H, D]})
+                  dict(CONFIGS["head_fp8_learned"], act=[T, H, D]))
     wl.ops = [Op("qdq_fwd per-head fp8", "fp8_head_fwd", n, 4 * n,
                  lambda st: aqfq.aqfq_qdq_fwd(sp, x, s, None, y, stream=st)),
               Op("scale_grad per-head fp8 (+dx)", "fp8_head_grad", n, 6 * n,
@@ -305,7 +332,7 @@ def int8_channel(dev, seed=0):
     y, ds = torch.empty_like(w), torch.empty_like(s)
     n = w.numel()
     wl = Workload("int8_channel", "INT8 per-channel weight [256,512]",
-                  {"workload": "int8_per_channel_weight", "w": [256, 512]})
+                  dict(CONFIGS["int8_channel"]))
     wl.ops = [Op("qdq_fwd int8", "int8_fwd", n, 4 * n + 4 * w.shape[1],
                  lambda st: aqfq.aqfq_qdq_fwd(sp, w, s, None, y, stream=st)),
               Op("scale_grad int8", "int8_grad", n, 4 * n + 8 * w.shape[1],
@@ -351,8 +378,7 @@ def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8, experts=None):
 
     wl = Workload("grouped_nvfp4_gemm",
                   "fused NVFP4 weight fake-quant + grouped GEMM, X [65536,2048] x W [128,1536,2048]",
-                  {"workload": "grouped_nvfp4_gemm_gate_up", "x": [M, K], "w": [E, N, K],
-                   "routing": "multinomial, expert popularity exp(N(0,0.3^2))"})
+                  dict(CONFIGS["grouped_nvfp4_gemm"], x=[M, K], w=[E, N, K]))
     wl.ops = [Op("fused qdq+grouped gemm", "qdq_gemm", M * N, flops,
                  lambda st: aqfq.aqfq_grouped_qdq_gemm(x, offd, w, s, g, y, err, stream=st))]
     wl.reference_ops = [Op("unfused: qdq stack + per-expert cuBLAS", "qdq_then_cublas", M * N, flops,
@@ -376,10 +402,7 @@ def _kd(name, kd_type, topk, dev, seed=0, T=synth.KD_TOKENS, V=synth.KD_VOCAB):
     n = T * V
     label = {aqfq.KD_CAKLD: "cakld", aqfq.KD_KL: "kl", aqfq.KD_RKL: "rkl", aqfq.KD_MSE: "mse"}[kd_type]
     wl = Workload(name, f"distillation loss {label}{f' top-{topk}' if topk else ''}, logits [{T}, {V}]",
-                  {"workload": f"kd_{label}{f'_top{topk}' if topk else ''}_logits", "logits": [T, V],
-                   "loss": label, "topk": topk,
-                   "logits_recipe": "teacher N(0,4) + one favoured token +U(4,12); student = teacher "
-                                    "+ N(0,0.09); 10% ignored positions"})
+                  dict(CONFIGS[name], logits=[T, V]))
     # algorithmic bytes: both logit rows read and the gradient row written at
     # each valid position; only the (zero) gradient row at an ignored one
     n_valid = int(((labels >= 0) & (labels < V)).sum())
