@@ -14,15 +14,17 @@
 // averaged over the valid positions; the gradient of that mean times
 // grad_scale is written for the student logits.
 //
-// Layout of the work: one cluster of 16 CTAs per position, two CTAs per SM.
-// CTA r holds the vocabulary slice [r S, r S + S) of both rows in shared
-// memory; a bulk copy (TMA, one per tensor) brings the next position's slice
-// into the other of two buffers while the current one is processed, so HBM
-// sees each logit once and each gradient element once and stays busy through
-// the cluster barriers.  Row statistics (max and sum of exponentials), the
-// top-K histograms and the loss sums are combined across the cluster through
-// distributed shared memory, always in rank order, so every CTA holds
-// bit-identical row values and results are reproducible.
+// Layout of the work: one cluster of 8 CTAs per position (persistent over
+// positions), 256 threads each: three CTAs per SM for the whole vocabulary of
+// a Qwen3-sized model.  CTA r holds the vocabulary slice [r S, r S + S) of
+// both rows in shared memory, brought in by two bulk copies (TMA, mbarrier)
+// issued as soon as the previous position has released the buffer, so HBM
+// sees each logit once and each gradient element once; the other CTAs of the
+// SM compute while one waits.  The row statistics (max and sum of
+// exponentials) and the top-K histograms are combined across the cluster
+// through distributed shared memory in a fixed order, so every CTA holds
+// bit-identical row values; each slice's loss sums go to the workspace and
+// a second kernel adds them in rank order: results are reproducible.
 //
 // Top-K support: 16-bit order-preserving keys of the teacher's BF16 values.
 // The K-th largest element is at least the K-th largest of the 8-element
@@ -58,7 +60,10 @@ using sm100::smem_u32;
 #endif
 constexpr int kCl = AQFQ_KD_CLUSTER;  // CTAs per position (vocabulary slices)
 constexpr int kNbuf = AQFQ_KD_NBUF;   // slice buffers per CTA
-constexpr int kThr = 512;       // threads per CTA
+#ifndef AQFQ_KD_THREADS
+#define AQFQ_KD_THREADS 256
+#endif
+constexpr int kThr = AQFQ_KD_THREADS;  // threads per CTA
 constexpr int kWarps = kThr / 32;
 constexpr int kHist1 = 4096;    // bins: the top 12 bits of the 16-bit teacher key
 constexpr int kHistWords = kHist1 / 2;  // two 16-bit counters per word (a slice has < 2^16 elements)
@@ -82,16 +87,23 @@ struct KdArgs {
   float tau, tau2, grad_scale;
 };
 
+// Per-CTA bookkeeping, kept small: with the Qwen3-sized vocabulary the
+// whole-vocabulary layout (slices + this) fits three CTAs per SM when the
+// thread count allows it.
 struct __align__(16) KdShared {
   uint64_t full[2];         // mbarriers of the two slice buffers
-  float xw[2][12];          // this CTA's reduction record (alternating exchange slots)
-  float red[kWarps][12];    // block reductions
+  float xw[2][10];          // this CTA's reduction record (alternating exchange slots)
+  float red[kWarps][9];     // per-warp records; per-warp loss sums in [w][0..1]
   int32_t ired[kWarps + 1];
-  uint32_t hist2[16];       // low nibble of the keys in the threshold bin
-  uint32_t h2all[kCl][16];  // hist2 of every rank
   int32_t sel[8];           // threshold search results
   int32_t err;
   float res[10];            // the last reduction's result, for every thread
+};
+
+// top-K only (dynamic shared memory after the histograms)
+struct __align__(16) TopkShared {
+  uint32_t hist2[16];       // low nibble of the keys in the threshold bin
+  uint32_t h2all[kCl][16];  // hist2 of every rank
   uint32_t bins[32];        // cluster-wide counts of 32 histogram bins
 };
 
@@ -370,7 +382,7 @@ __device__ __forceinline__ int block_scan(int v, int& total, KdShared* sh) {
 // fewer than K.  All threads call it.  Each step covers 32 bins: thread t
 // loads bin t / 16 of the step from rank t % 16 (one remote load each).
 __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int K, int& bin,
-                                              int& above, KdShared* sh) {
+                                              int& above, KdShared* sh, TopkShared* tk) {
   static_assert(kThr >= 32 * kCl && kCl <= 32, "one remote load per thread per 32-bin step");
   const int tid = threadIdx.x, j = tid / kCl, r = tid % kCl;
   const bool part = tid < 32 * kCl;
@@ -382,10 +394,10 @@ __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int
                      : 0u;
 #pragma unroll
     for (int d = kCl / 2; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
-    if (part && r == 0) sh->bins[j] = c;
+    if (part && r == 0) tk->bins[j] = c;
     __syncthreads();
     if (tid < 32) {  // one warp scans the 32 bins from the top
-      const int cj = int(sh->bins[tid]);
+      const int cj = int(tk->bins[tid]);
       int x = cj;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -451,13 +463,15 @@ __device__ __forceinline__ void ordered_scan(const uint16_t* tsl, const uint16_t
 //          2^(x_s - m) (x_s - x_t) for the reverse KL that centres it
 //   MSE    mean squared error loss and gradient
 template <bool TOPK, bool RGRAD, bool MSE>
-__global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
+__global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(const KdArgs a) {
   extern __shared__ __align__(16) uint8_t kd_smem[];
   KdShared* sh = reinterpret_cast<KdShared*>(kd_smem);
   const int nvb = TOPK ? (a.S / 8 + 7) / 8 * 8 : 0;  // vector slots, padded to 16 bytes
   uint32_t* vhist = reinterpret_cast<uint32_t*>(kd_smem + sizeof(KdShared));  // vector-max bins
   uint32_t* hist1 = vhist + (TOPK ? kHistWords : 0);                           // element bins
-  uint16_t* vbin = reinterpret_cast<uint16_t*>(hist1 + (TOPK ? kHistWords : 0));  // bin of each vector max
+  TopkShared* tk = reinterpret_cast<TopkShared*>(hist1 + (TOPK ? kHistWords : 0));
+  uint16_t* vbin = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(tk) +
+                                               (TOPK ? sizeof(TopkShared) : 0));  // bin of each vector max
   uint16_t* cand = vbin + nvb;                                                 // candidate vectors
   uint16_t* buf0 = cand + nvb;  // kNbuf buffers of [teacher S | student S]
   const int tid = threadIdx.x, lane = tid & 31;
@@ -483,7 +497,7 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
   }
   if (TOPK) {
     for (int i = tid; i < 2 * kHistWords; i += kThr) vhist[i] = 0;
-    if (tid < 16) sh->hist2[tid] = 0;
+    if (tid < 16) tk->hist2[tid] = 0;
   }
   __syncthreads();
 
@@ -624,7 +638,7 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     if (TOPK) {
       const int top = kmax >> 4;
       int b0 = 0, above = 0;
-      if (!find_from_top(vhist, top, a.K, b0, above, sh)) b0 = 0;
+      if (!find_from_top(vhist, top, a.K, b0, above, sh, tk)) b0 = 0;
       {  // candidate vectors (maximum at or above the bound), ascending: a
          // contiguous range of vectors per thread and one block scan
         const int per = (nvec + kThr - 1) / kThr, v0t = tid * per;
@@ -650,7 +664,7 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
       __syncthreads();
       cluster_sync();
       int bstar = 0;
-      find_from_top(hist1, top, a.K, bstar, above, sh);  // holds at least K
+      find_from_top(hist1, top, a.K, bstar, above, sh, tk);  // holds at least K
       const int need = a.K - above;
       for (int p = tid; p < nc; p += kThr) {
         const int v = cand[p];
@@ -659,26 +673,26 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t k = key_of(w, j);
-          if (int(k >> 4) == bstar) atomicAdd(&sh->hist2[k & 15u], 1u);
+          if (int(k >> 4) == bstar) atomicAdd(&tk->hist2[k & 15u], 1u);
         }
       }
       __syncthreads();
       cluster_sync();
       if (tid < kCl * 16)
-        sh->h2all[tid >> 4][tid & 15] = ld_remote_u32(remote_addr(&sh->hist2[tid & 15], tid >> 4));
+        tk->h2all[tid >> 4][tid & 15] = ld_remote_u32(remote_addr(&tk->hist2[tid & 15], tid >> 4));
       __syncthreads();
       if (tid == 0) {
         int cum = 0, l = 15;
         for (; l > 0; --l) {
           int h = 0;
-          for (int r = 0; r < kCl; ++r) h += int(sh->h2all[r][l]);
+          for (int r = 0; r < kCl; ++r) h += int(tk->h2all[r][l]);
           if (cum + h >= need) break;
           cum += h;
         }
         const int q = need - cum;  // elements equal to the threshold key to take
         int before = 0;
-        for (uint32_t r = 0; r < rank; ++r) before += int(sh->h2all[r][l]);
-        const int eq = int(sh->h2all[rank][l]);
+        for (uint32_t r = 0; r < rank; ++r) before += int(tk->h2all[r][l]);
+        const int eq = int(tk->h2all[rank][l]);
         int take = q - before;
         take = take < 0 ? 0 : (take > eq ? eq : take);
         sh->sel[2] = int((uint32_t(bstar) << 4) | uint32_t(l));
@@ -803,8 +817,8 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
         r = __fadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, d));
       }
       if (lane == 0) {
-        sh->red[tid >> 5][10] = f;
-        sh->red[tid >> 5][11] = r;
+        sh->red[tid >> 5][0] = f;
+        sh->red[tid >> 5][1] = r;
       }
     }
     if (TOPK && a.topk_idx) {  // the support in ascending vocabulary order
@@ -822,8 +836,8 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     if (tid == 0) {
       float F = 0.0f, R = 0.0f;
       for (int k = 0; k < kWarps; ++k) {
-        F = __fadd_rn(F, sh->red[k][10]);
-        R = __fadd_rn(R, sh->red[k][11]);
+        F = __fadd_rn(F, sh->red[k][0]);
+        R = __fadd_rn(R, sh->red[k][1]);
       }
       a.part[(row * kCl + rank) * 2] = F;
       a.part[(row * kCl + rank) * 2 + 1] = R;
@@ -841,7 +855,7 @@ __global__ void __launch_bounds__(kThr, 2) kd_loss_kernel(const KdArgs a) {
     }
     if (TOPK) {  // peers read these before the support-statistics exchange
       for (int i = tid; i < 2 * kHistWords; i += kThr) vhist[i] = 0;
-      if (tid < 16) sh->hist2[tid] = 0;
+      if (tid < 16) tk->hist2[tid] = 0;
     }
     __syncthreads();
   }
@@ -937,7 +951,8 @@ size_t ws_part_bytes(int64_t T) { return (size_t(T) * kCl * 8 + 255) / 256 * 256
 
 size_t kd_smem_bytes(int32_t S, bool topk) {
   const size_t vbin = topk ? size_t((S / 8 + 7) / 8 * 8) * 4 : 0;  // vector bins + candidate list
-  return sizeof(KdShared) + (topk ? size_t(2 * kHistWords) * 4 : 0) + vbin + size_t(S) * 4 * kNbuf;
+  return sizeof(KdShared) + (topk ? size_t(2 * kHistWords) * 4 + sizeof(TopkShared) : 0) + vbin +
+         size_t(S) * 4 * kNbuf;
 }
 
 int max_smem_optin() {
