@@ -311,6 +311,14 @@ aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void* teacher,
                          void* dstudent, int32_t* topk_idx, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Diagnostic (the pages have no counterpart): checks the bounded-wait path
+ * that the GEMM's pipeline uses when a stage never arrives.  One thread waits
+ * on an mbarrier phase that nothing completes, polling at most `polls` times
+ * (1 <= polls <= 2^22, backing off to 256 ns per poll), then sets *flag = 1
+ * (device int32, 4-byte aligned) and returns; the context stays usable.
+ * Asynchronous on `stream`; allocates nothing. */
+aqfq_status aqfq_selftest_wait_timeout(int32_t* flag, uint32_t polls, void* stream);
+
 /* Static text for a status code. */
 const char* aqfq_status_string(aqfq_status status);
 

@@ -31,8 +31,8 @@ STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_AL
 EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_grouped_qdq_gemm", "aqfq_scale_grad",
            "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
-           "aqfq_scale_init", "aqfq_kd_loss", "aqfq_kd_workspace_bytes", "aqfq_status_string",
-           "aqfq_version")
+           "aqfq_scale_init", "aqfq_kd_loss", "aqfq_kd_workspace_bytes",
+           "aqfq_selftest_wait_timeout", "aqfq_status_string", "aqfq_version")
 
 
 class QSpec(ctypes.Structure):
@@ -76,6 +76,7 @@ def lib():
                 "aqfq_kd_loss": (i32, [i32, P, P, P, i64, i64, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_float, P, P, P, P, P, sz, P]),
                 "aqfq_kd_workspace_bytes": (sz, [i64]),
+                "aqfq_selftest_wait_timeout": (i32, [P, ctypes.c_uint32, P]),
                 "aqfq_status_string": (ctypes.c_char_p, [i32]),
                 "aqfq_version": (i32, []),
             }
@@ -166,6 +167,15 @@ def aqfq_grouped_qdq_gemm(x, m_offsets, w, scale, tensor_scale, y, error_flag=No
                                      _ptr(tensor_scale), E, N, K, _ptr(y), _ptr(error_flag),
                                      _stream(stream))
     _check("aqfq_grouped_qdq_gemm", st)
+
+
+def aqfq_selftest_wait_timeout(flag, polls, stream=None):
+    """Diagnostic: a bounded device wait that nothing completes sets flag (int32
+    device tensor) to 1 after `polls` polls."""
+    if flag.dtype != torch.int32:
+        raise TypeError("flag must be int32")
+    _check("aqfq_selftest_wait_timeout",
+           lib().aqfq_selftest_wait_timeout(_ptr(flag), int(polls), _stream(stream)))
 
 
 def aqfq_kd_workspace_bytes(T) -> int:

@@ -321,6 +321,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0 && aborted(sh) && a.err) atomicExch(a.err, 1);
 }
 
+// Diagnostic: one thread waits, through the same bounded wait as the GEMM's
+// pipeline, for a barrier phase that nothing completes; when the wait gives
+// up it raises *flag (the GEMM's timeout path sets its error flag the same way).
+__global__ void wait_timeout_kernel(int32_t* flag, uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait(&bar, 0, polls)) atomicExch(flag, 1);
+}
+
 // ---- host side -------------------------------------------------------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -396,5 +407,14 @@ extern "C" aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_off
   dim3 grid(unsigned(N / BN), unsigned(slots), 1);
   grouped_qdq_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, static_cast<cudaStream_t>(stream)>>>(tm,
                                                                                                 a);
+  return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
+}
+
+extern "C" aqfq_status aqfq_selftest_wait_timeout(int32_t* flag, uint32_t polls, void* stream) {
+  using namespace aqfq;
+  if (!flag) return AQFQ_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(flag) & 3) != 0) return AQFQ_ERR_ALIGN;
+  if (polls == 0 || polls > kWaitPolls) return AQFQ_ERR_SHAPE;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(flag, polls);
   return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
 }

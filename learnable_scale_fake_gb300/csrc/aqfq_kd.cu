@@ -234,16 +234,18 @@ __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
                : "memory");
 }
 
-// (max, sum of 2^(x - max), weighted sum) of a set; z == 0 marks an empty set.
+// A set of logits v, kept in raw (BF16) units so that every exponent is a
+// difference of nearby values: m = max v, z = sum 2^((v - m) ks), b = a
+// weighted sum under the same weights; z == 0 marks an empty set.
 struct Online {
   float m, z, b;
 };
 __device__ __forceinline__ Online online_empty() { return Online{-INFINITY, 0.0f, 0.0f}; }
 // symmetric in its operands (bit for bit), so butterfly lanes agree
-__device__ __forceinline__ Online online_merge(Online a, Online c) {
+__device__ __forceinline__ Online online_merge(Online a, Online c, float ks) {
   const float m = fmaxf(a.m, c.m);
-  const float fa = a.z != 0.0f ? ex2(a.m - m) : 0.0f;
-  const float fc = c.z != 0.0f ? ex2(c.m - m) : 0.0f;
+  const float fa = a.z != 0.0f ? ex2(__fmul_rn(__fsub_rn(a.m, m), ks)) : 0.0f;
+  const float fc = c.z != 0.0f ? ex2(__fmul_rn(__fsub_rn(c.m, m), ks)) : 0.0f;
   return Online{m, __fadd_rn(__fmul_rn(a.z, fa), __fmul_rn(c.z, fc)),
                 __fadd_rn(__fmul_rn(a.b, fa), __fmul_rn(c.b, fc))};
 }
@@ -280,8 +282,8 @@ struct Rec {
 };
 __device__ __forceinline__ Rec rec_empty() { return Rec{online_empty(), online_empty(), 0.0f, 0.0f, 0}; }
 template <bool KMAX>
-__device__ __forceinline__ Rec rec_merge(const Rec& a, const Rec& c) {
-  return Rec{online_merge(a.t, c.t), online_merge(a.s, c.s), __fadd_rn(a.u, c.u),
+__device__ __forceinline__ Rec rec_merge(const Rec& a, const Rec& c, float ks) {
+  return Rec{online_merge(a.t, c.t, ks), online_merge(a.s, c.s, ks), __fadd_rn(a.u, c.u),
              __fadd_rn(a.v, c.v), KMAX ? max(a.k, c.k) : a.k + c.k};
 }
 __device__ __forceinline__ Rec rec_shfl(const Rec& a, int d) {
@@ -291,9 +293,9 @@ __device__ __forceinline__ Rec rec_shfl(const Rec& a, int d) {
 // xor butterfly over the warp: every lane ends with the same total (the merge
 // is symmetric bit for bit), in a fixed order
 template <bool KMAX>
-__device__ __forceinline__ Rec warp_rec(Rec a) {
+__device__ __forceinline__ Rec warp_rec(Rec a, float ks) {
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) a = rec_merge<KMAX>(a, rec_shfl(a, d));
+  for (int d = 16; d >= 1; d >>= 1) a = rec_merge<KMAX>(a, rec_shfl(a, d), ks);
   return a;
 }
 __device__ __forceinline__ void rec_store(float* p, const Rec& a) {
@@ -315,14 +317,14 @@ __device__ __forceinline__ Rec rec_load(const float* p) {
 // warp records and the result are rewritten only after barriers that every
 // thread reaches after reading them.
 template <bool KMAX>
-__device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par,
+__device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par, float ks,
                                            int* k_before = nullptr) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) rec_store(sh->red[w], wr);
   __syncthreads();
   if (w == 0) {
     Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
-    x = warp_rec<KMAX>(x);
+    x = warp_rec<KMAX>(x, ks);
     if (l == 0) rec_store(sh->xw[par], x);
   }
   cluster_sync();
@@ -344,7 +346,7 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
       }
       if (uint32_t(l) == cluster_rank()) sh->res[9] = __int_as_float(inc - x.k);
     }
-    x = warp_rec<KMAX>(x);
+    x = warp_rec<KMAX>(x, ks);
     if (l == 0) rec_store(sh->res, x);
   }
   __syncthreads();
@@ -557,11 +559,10 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
     const int64_t lloc = int64_t(a.labels[row]) - v0;  // the label's index within the slice
 
     // ---- pass 1: whole-vocabulary statistics (teacher; student unless TOPK) --
-    // One read of each vector: per-thread running maxima of the scaled values,
-    // the sums rescaled when a vector raises them; warps then merge by
-    // butterfly and the cluster merges the warps' records.
-    float tmax = -INFINITY, smax = -INFINITY;  // raw (BF16) maxima
-    float mt = -INFINITY, ms = -INFINITY;      // scaled maxima: the sums' reference
+    // One read of each vector: per-thread running maxima (raw units), the
+    // sums of 2^((v - max) ks) rescaled when a vector raises them; warps then
+    // merge by butterfly and the cluster merges the warps' records.
+    float tmax = -INFINITY, smax = -INFINITY;  // raw (BF16) maxima: the sums' reference
     f2 zt = 0, zs = 0, bb = 0, se2 = 0;
     {
       const f2 KS = mk2(ks, ks);
@@ -574,33 +575,31 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
           atomicAdd(&vhist[kb >> 1], 1u << ((kb & 1u) * 16));
         }
         if (vt > tmax) {
-          tmax = vt;
-          const float m = __fmul_rn(vt, ks), f = ex2(mt - m);
+          const float f = ex2(__fmul_rn(__fsub_rn(tmax, vt), ks));
           zt = mul2(zt, mk2(f, f));
-          mt = m;
+          tmax = vt;
         }
-        const f2 NMT = mk2(-mt, -mt);
+        const f2 TM = mk2(tmax, tmax);
         uint4 x = make_uint4(0, 0, 0, 0);
-        f2 NMS = 0;
+        f2 SM = 0;
         if (!TOPK) {
           x = s4[v];
           const float vs = vmax8(x);
           if (vs > smax) {
-            smax = vs;
-            const float m = __fmul_rn(vs, ks), f = ex2(ms - m);
+            const float f = ex2(__fmul_rn(__fsub_rn(smax, vs), ks));
             zs = mul2(zs, mk2(f, f));
             if (RGRAD) bb = mul2(bb, mk2(f, f));
-            ms = m;
+            smax = vs;
           }
-          NMS = mk2(-ms, -ms);
+          SM = mk2(smax, smax);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const f2 t2 = bf2(word(w, i));
-          zt = add2(zt, ex2x2(fma2(t2, KS, NMT)));
+          zt = add2(zt, ex2x2(mul2(sub2(t2, TM), KS)));
           if (!TOPK) {
             const f2 s2 = bf2(word(x, i));
-            const f2 es = ex2x2(fma2(s2, KS, NMS));
+            const f2 es = ex2x2(mul2(sub2(s2, SM), KS));
             zs = add2(zs, es);
             if (RGRAD || MSE) {
               const f2 d = sub2(s2, t2);
@@ -611,26 +610,26 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
         }
       }
     }
-    // the label's scaled teacher value, from the thread whose vectors hold it
+    // the label's teacher logit (raw), from the thread whose vectors hold it
     const bool owns_label = lloc >= 0 && lloc < n64 && int((lloc >> 3) % kThr) == tid;
-    const float xl = owns_label ? __fmul_rn(__uint_as_float(uint32_t(tsl[lloc]) << 16), ks) : 0.0f;
-    const Rec mine{Online{mt, __fadd_rn(lo2(zt), hi2(zt)), 0.0f},
-                   Online{ms, __fadd_rn(lo2(zs), hi2(zs)), __fmul_rn(__fadd_rn(lo2(bb), hi2(bb)), ks)},
+    const float xl = owns_label ? __uint_as_float(uint32_t(tsl[lloc]) << 16) : 0.0f;
+    const Rec mine{Online{tmax, __fadd_rn(lo2(zt), hi2(zt)), 0.0f},
+                   Online{smax, __fadd_rn(lo2(zs), hi2(zs)), __fmul_rn(__fadd_rn(lo2(bb), hi2(bb)), ks)},
                    __fadd_rn(lo2(se2), hi2(se2)), 0.0f,
                    (TOPK && tmax > -INFINITY) ? int(key_of_f(tmax)) : 0};
-    Rec wr = warp_rec<true>(mine);
+    Rec wr = warp_rec<true>(mine, ks);
     {  // the label's value: one thread of one CTA holds it; the butterfly adds zeros
       float x = xl;
 #pragma unroll
       for (int d = 16; d >= 1; d >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, d));
       wr.v = x;
     }
-    const Rec R1 = cluster_rec<true>(wr, sh, par);
+    const Rec R1 = cluster_rec<true>(wr, sh, par, ks);
     const Online T_ = R1.t, S_ = R1.s;
     const float SE = R1.u, XL = R1.v;
     const int kmax = R1.k;
     // conf: the whole-vocabulary teacher probability of the label
-    const float conf = ex2(XL - (T_.m + log2f(T_.z)));
+    const float conf = ex2(__fmaf_rn(__fsub_rn(XL, T_.m), ks, -log2f(T_.z)));
 
     // ---- top-K support: threshold key, ties by index ----------------------
     uint32_t tkey = 0;
@@ -639,6 +638,11 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
       const int top = kmax >> 4;
       int b0 = 0, above = 0;
       if (!find_from_top(vhist, top, a.K, b0, above, sh, tk)) b0 = 0;
+      // keys at or above the bound span few 12-bit bins: count exact 16-bit
+      // keys there (one histogram gives the threshold key and the per-rank
+      // ties); otherwise 12-bit bins, then the low 4 bits of the threshold bin
+      const bool exact = (top - b0 + 1) * 16 <= kHist1;
+      const uint32_t kbase = uint32_t(b0) << 4;
       {  // candidate vectors (maximum at or above the bound), ascending: a
          // contiguous range of vectors per thread and one block scan
         const int per = (nvec + kThr - 1) / kThr, v0t = tid * per;
@@ -652,17 +656,41 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
         nc = total;
         __syncthreads();
       }
-      // elements at or above the bound: 12-bit histogram
+      // elements at or above the bound: exact-key or 12-bit histogram
       for (int p = tid; p < nc; p += kThr) {
         const uint4 w = t4[cand[p]];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t k = key_of(w, j);
-          if (int(k >> 4) >= b0) atomicAdd(&hist1[k >> 5], 1u << (((k >> 4) & 1u) * 16));
+          if (int(k >> 4) >= b0) {
+            const uint32_t bin = exact ? k - kbase : (k >> 4);
+            atomicAdd(&hist1[bin >> 1], 1u << ((bin & 1u) * 16));
+          }
         }
       }
       __syncthreads();
       cluster_sync();
+      if (exact) {
+        int tb = 0;
+        find_from_top(hist1, int((uint32_t(top + 1) << 4) - 1 - kbase), a.K, tb, above, sh, tk);
+        const int need = a.K - above;  // elements equal to the threshold key to take
+        if (tid < kCl)
+          tk->h2all[tid][0] =
+              (ld_remote_u32(remote_addr(hist1 + (tb >> 1), uint32_t(tid))) >> ((tb & 1) * 16)) & 0xFFFFu;
+        __syncthreads();
+        if (tid == 0) {
+          int before = 0;
+          for (uint32_t r = 0; r < rank; ++r) before += int(tk->h2all[r][0]);
+          const int eq = int(tk->h2all[rank][0]);
+          int take = need - before;
+          take = take < 0 ? 0 : (take > eq ? eq : take);
+          sh->sel[2] = int(kbase + uint32_t(tb));
+          sh->sel[3] = take;
+          sh->sel[4] = eq;
+          sh->sel[5] = -1;
+        }
+        __syncthreads();
+      } else {
       int bstar = 0;
       find_from_top(hist1, top, a.K, bstar, above, sh, tk);  // holds at least K
       const int need = a.K - above;
@@ -701,6 +729,7 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
         sh->sel[5] = -1;
       }
       __syncthreads();
+      }
       tkey = uint32_t(sh->sel[2]);
       tbin = int(tkey >> 4);
       const int take = sh->sel[3], eq = sh->sel[4];
@@ -720,7 +749,9 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
     auto selected = [&](int i, uint32_t k) { return k > tkey || (k == tkey && i <= idx_lim); };
 
     // ---- statistics over the support -----------------------------------------
-    float lse_t, lse_s, rkl0;
+    // each distribution over the support as (raw maximum M, L = log2 of the
+    // sum of 2^((v - M) ks)): log2 p = (v - M) ks - L
+    float m_t, m_s, l_t, l_s, bz;
     int sel_before = 0;
     if (TOPK) {
       Online ut = online_empty(), us = online_empty();
@@ -735,27 +766,35 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
           const uint32_t tw = word(w, j >> 1), sw = word(x, j >> 1);
           const float t = __uint_as_float(j & 1 ? tw & 0xFFFF0000u : tw << 16);
           const float s = __uint_as_float(j & 1 ? sw & 0xFFFF0000u : sw << 16);
-          ut = online_merge(ut, Online{__fmul_rn(t, ks), 1.0f, 0.0f});
-          us = online_merge(us, Online{__fmul_rn(s, ks), 1.0f, __fmul_rn(__fsub_rn(s, t), ks)});
+          ut = online_merge(ut, Online{t, 1.0f, 0.0f}, ks);
+          us = online_merge(us, Online{s, 1.0f, __fmul_rn(__fsub_rn(s, t), ks)}, ks);
           ++cnt;
         }
       }
-      const Rec RS = cluster_rec<false>(warp_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}), sh, par,
-                                        &sel_before);
-      lse_t = RS.t.m + log2f(RS.t.z);
-      lse_s = RS.s.m + log2f(RS.s.z);
-      rkl0 = kLn2 * (RS.s.b / RS.s.z - (lse_s - lse_t));
+      const Rec RS = cluster_rec<false>(warp_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}, ks), sh, par,
+                                        ks, &sel_before);
+      m_t = RS.t.m;
+      m_s = RS.s.m;
+      l_t = log2f(RS.t.z);
+      l_s = log2f(RS.s.z);
+      bz = RS.s.b / RS.s.z;
     } else {
-      lse_t = T_.m + log2f(T_.z);
-      lse_s = S_.m + log2f(S_.z);
-      rkl0 = kLn2 * (S_.b / S_.z - (lse_s - lse_t));
+      m_t = T_.m;
+      m_s = S_.m;
+      l_t = log2f(T_.z);
+      l_s = log2f(S_.z);
+      bz = S_.b / S_.z;
     }
 
     // ---- pass 2: loss terms and the gradient ---------------------------------
-    const float dl = lse_t - lse_s;
+    // dl = log2 of the normalisers' ratio (teacher over student), in base-2 units;
+    // rkl0 = sum p_s (log p_s - log p_t) in nats (centres the reverse-KL gradient)
+    const float dl = __fmaf_rn(__fsub_rn(m_t, m_s), ks, __fsub_rn(l_t, l_s));
+    const float rkl0 = kLn2 * (bz + dl);
     const float wf = a.type == AQFQ_KD_KL ? 1.0f : a.type == AQFQ_KD_RKL ? 0.0f : 1.0f - conf;
     const float wr2 = a.type == AQFQ_KD_KL ? 0.0f : a.type == AQFQ_KD_RKL ? 1.0f : conf;
-    const f2 KS = mk2(ks, ks), NLT = mk2(-lse_t, -lse_t), NLS = mk2(-lse_s, -lse_s);
+    const f2 KS = mk2(ks, ks), NLT = mk2(-l_t, -l_t), NLS = mk2(-l_s, -l_s);
+    const f2 MT = mk2(m_t, m_t), MS = mk2(m_s, m_s);
     const float kl = ks * kLn2, ndl = -dl * kLn2;
     const f2 KL2 = mk2(kl, kl), NDL = mk2(ndl, ndl);
     // gradient: gsc (wf (p_s - p_t) - wr p_s (d + rkl)) = p_s (c - gsc wr d) - gsc wf p_t
@@ -772,7 +811,7 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const f2 t2 = bf2(word(w, i)), s2 = bf2(word(x, i));
-        f2 pt = ex2x2(fma2(t2, KS, NLT)), ps = ex2x2(fma2(s2, KS, NLS));
+        f2 pt = ex2x2(fma2(sub2(t2, MT), KS, NLT)), ps = ex2x2(fma2(sub2(s2, MS), KS, NLS));
         if (masked) {  // zero outside the support
           const bool in0 = selected(8 * v + 2 * i, key_of(w, 2 * i));
           const bool in1 = selected(8 * v + 2 * i + 1, key_of(w, 2 * i + 1));

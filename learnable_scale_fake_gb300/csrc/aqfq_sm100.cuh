@@ -53,8 +53,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete; gives up after a
 // bounded number of polls (about a second with the back-off) and returns false.
 constexpr uint32_t kWaitPolls = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_test(bar, parity)) return true;
     if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
   }

@@ -190,3 +190,10 @@ def test_kd_loss_host_checks(L):
     assert kd(L, tl=6 * A + 2) == ALIGN
     assert aqfq.aqfq_kd_workspace_bytes(0) == 256
     assert aqfq.aqfq_kd_workspace_bytes(4096) >= 256 + 12 * 4096
+
+
+def test_selftest_wait_timeout_host_checks(L):
+    assert L.aqfq_selftest_wait_timeout(None, 16, None) == NULL
+    assert L.aqfq_selftest_wait_timeout(A + 2, 16, None) == ALIGN
+    assert L.aqfq_selftest_wait_timeout(A, 0, None) == SHAPE
+    assert L.aqfq_selftest_wait_timeout(A, (1 << 22) + 1, None) == SHAPE

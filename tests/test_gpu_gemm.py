@@ -84,3 +84,17 @@ def test_gemm_argument_checks():
     y = torch.empty((16, 96), dtype=torch.bfloat16, device=d)
     with pytest.raises(aqfq.AqfqError):
         aqfq.aqfq_grouped_qdq_gemm(x, off, w, s, g, y)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A device wait that nothing completes gives up after its poll limit and
+    raises the flag; the context stays usable (a GEMM right after is exact)."""
+    d = dev()
+    flag = torch.zeros(1, dtype=torch.int32, device=d)
+    aqfq.aqfq_selftest_wait_timeout(flag, 1 << 12)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
+    x, off, w, s, g = _inputs(1, 128, 64, [128], 201, onehot=True)
+    y = _run(x, off, w, s, g)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), s.numpy(), g.numpy())
+    assert np.array_equal(bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16)))

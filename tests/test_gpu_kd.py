@@ -194,3 +194,17 @@ def test_full_size_bench_workload(name):
     assert np.all(np.abs(gds - sub["dstudent"]) <= ds_tol)
     if topk:
         np.testing.assert_array_equal(idx[rows].cpu().numpy(), sub["topk_idx"])
+
+
+def test_topk_wide_key_range_two_level_path():
+    """Teacher logits spread over 120 octaves (both signs): the keys above the
+    vector-max bound span more bins than the exact-key histogram holds, so the
+    12-bit + 4-bit path decides the threshold; small and large K."""
+    rng = np.random.default_rng(31)
+    T, V = 5, 16384
+    mag = np.exp2(rng.uniform(-60, 60, (T, V))).astype(np.float32)
+    t = torch.from_numpy(mag * rng.choice([-1.0, 1.0], (T, V)).astype(np.float32)).bfloat16()
+    s = (t.float() * 0.5 + torch.from_numpy(rng.normal(size=(T, V)).astype(np.float32))).bfloat16()
+    lab = rng.integers(0, V, T)
+    for K in (5, 50, 700):
+        check(O.KD_RKL, s, t, lab, topk=K, want_idx=True)
