@@ -9,19 +9,28 @@
 // One CTA computes up to MT = 4 output tiles of 128 x 128 of one expert that
 // share a column tile, K in steps of 64; the fake-quantized weight tile of a
 // step feeds all of them (the fake-quant work per FLOP falls by the number of
-// row tiles):
-//   warp 0      TMA producer: X tiles [128 rows, 64] -> shared (128-byte swizzle)
+// row tiles).  Warp w runs on scheduler w % 4; the MMA issuer shares its
+// scheduler with no fake-quant warp (arithmetic-heavy warps beside it starve
+// its issue slots and stall the tensor pipe):
 //   warp 1      allocates the 512 TMEM columns (4 FP32 accumulators of 128 x
 //               128); one lane issues tcgen05.mma (kind::f16, M=128, N=128,
 //               K=16; 4 K-slices x up to 4 row tiles per step) and commits
-//   warps 2-9   weight producers: load W chunks + block scales, fake-quantize
+//   warp 5      TMA producer: X tiles [128 rows, 64] -> shared (128-byte swizzle)
+//   warps 2-4, 6-8, 10, 11
+//               weight producers: load W chunks + block scales, fake-quantize
 //               them (the same chunk arithmetic as aqfq_qdq_fwd) and store the
-//               BF16 tile into shared memory in the 128-byte swizzle layout;
-//               then the epilogue (TMEM -> registers -> BF16 -> Y), two warps
-//               per TMEM lane quarter
-// A 2-stage ring of (4 X tiles, 1 W_hat tile) = 80 KiB per stage; full barriers
-// count the TMA bytes plus one arrival per producer warp, empty barriers are
+//               BF16 tile into shared memory in the 128-byte swizzle layout
+//   warps 4-11  epilogue (TMEM -> registers -> BF16 -> Y), two warps per TMEM
+//               lane quarter (warp 0 sets up the barriers)
+// Two rings: X (2 stages of 4 tiles, 64 KiB each; full barriers count the TMA
+// bytes) and W_hat (4 stages of 16 KiB; one arrival per producer warp), so the
+// producers can run up to three k-steps ahead of the MMAs; empty barriers are
 // armed by tcgen05.commit.
+// The CTAs of a cluster (kCN column tiles of the same row group) read the same
+// X tiles: each loads every kCN-th tile and multicasts it to all of them, and
+// every CTA's MMA commit releases an X stage in all of them (an X stage is
+// refilled only once every CTA has consumed it).  This divides the L2 -> SM
+// traffic for X, which otherwise paces the loads, by kCN.
 // Every wait is bounded; on a timeout the CTA drains what it issued, frees
 // its tensor memory, raises the caller's error flag and returns.
 #include <cuda.h>
@@ -37,13 +46,19 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 2, MT = 4;
-constexpr int kGemmThreads = 320;  // 10 warps
+constexpr int BM = 128, BN = 128, BK = 64, MT = 4;
+constexpr int XS = 2;  // X ring stages (MT tiles of 16 KiB each)
+constexpr int WS = 4;  // fake-quantized weight ring stages (16 KiB each)
+constexpr int kCN = 2;  // CTAs per cluster: column tiles of one row group share X
+constexpr int kGemmThreads = 384;  // 12 warps
+constexpr int kMmaWarp = 1, kTmaWarp = 5;
 constexpr int kProducerThreads = 256;
 constexpr uint32_t kTileBytes = BM * BK * 2;             // 16 KiB, one operand tile
 constexpr uint32_t kStageA = MT * kTileBytes;            // 64 KiB of X per stage
 constexpr uint32_t kTmemCols = MT * BN;                  // 512 columns
-constexpr size_t kGemmSmem = 1024 + STAGES * (kStageA + kTileBytes) + 256;
+constexpr size_t kScaleTab = 128 * 8;  // {S_hat, 1/S_hat} per non-negative E4M3 code
+constexpr size_t kRings = size_t(XS) * kStageA + size_t(WS) * kTileBytes;  // 192 KiB
+constexpr size_t kGemmSmem = 1024 + kRings + 256 + kScaleTab;
 
 struct GemmArgs {
   const uint8_t* w;       // [E, N, K] BF16
@@ -57,13 +72,49 @@ struct GemmArgs {
 };
 
 struct __align__(8) GemmShared {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full_x[XS], empty_x[XS];  // TMA bytes / MMA commit
+  uint64_t full_w[WS], empty_w[WS];  // one arrival per producer warp / MMA commit
   uint64_t accum;
   uint32_t tmem;
   int32_t abort;
   int32_t expert, mtile;
 };
+
+// ---- cluster forms of the TMA load and the MMA commit ------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2D tile load written to the same shared-memory offset of every CTA in
+// `mask`, completion counted on the mbarrier at the same offset in each
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* tmap, uint64_t* bar,
+                                               int32_t c0, int32_t c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+// one arrival, once this thread's prior tcgen05 operations complete, on the
+// mbarrier at the same offset in every CTA of `mask`
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
 
 __device__ __forceinline__ void set_abort(GemmShared* sh) {
   atomicExch(&sh->abort, 1);
@@ -108,17 +159,98 @@ __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int sl
   *mt_out = 0;
 }
 
+// ---- weight fake-quant in the producers ------------------------------------
+// The same values as aqfq_qdq_fwd's NVFP4 chunk arithmetic, arranged for
+// issue throughput (the producers' instruction count paces the main loop):
+// the expert's 256 possible block scales S_hat = RN(dec(e) g) and their
+// reciprocals come from a table built once per CTA, the block-scale quotient
+// S_b / g uses Markstein's correction with RN(1/g), and the per-element
+// division and dequantisation run as packed f32x2 operations (IEEE
+// round-to-nearest per lane, so every result is the scalar path's).
+
+// a pair of binary32 values in one 64-bit register (element 2i in the low half)
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 mk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(f2 v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi2(f2 v) { return __uint_as_float(uint32_t(v >> 32)); }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+struct ScaleEntry {
+  float s, r;  // S_hat and RN(1 / S_hat); r is NaN where the chunk takes the IEEE path
+};
+
+// S_hat for non-negative E4M3 code c and the reciprocal make_divisor would
+// form (its fast range [2^-64, 2^64]; outside it r = NaN, which fails the
+// chunk's range test)
+__device__ __forceinline__ ScaleEntry scale_entry(uint32_t c, float g) {
+  ScaleEntry e;
+  e.s = __fmul_rn(dec_e4m3x2(c).x, g);
+  const bool fast = (e.s >= 0x1p-64f) && (e.s <= 0x1p64f);
+  e.r = fast ? __frcp_rn(e.s) : __int_as_float(0x7FC00000);
+  return e;
+}
+
+// RN(S_b / g): q0 = RN(S_b rg), e = RN(S_b - q0 g) (exact), RN(q0 + e rg) is
+// the IEEE quotient whenever 2^-30 <= |q0| <= 2^100 and g lies in
+// [2^-64, 2^64] (rg = RN(1/g) there, NaN otherwise; ng = -g); every other case
+// divides.  g = 0 gives the zero quotient, as nvfp4_block_scale does.
+__device__ __forceinline__ float block_quotient(float sb, float g, float rg, float ng) {
+  const float q0 = __fmul_rn(sb, rg);
+  const float a = fabsf(q0);
+  if (a >= 0x1p-30f && a <= 0x1p100f) return __fmaf_rn(__fmaf_rn(q0, ng, sb), rg, q0);
+  return g != 0.0f ? __fdiv_rn(sb, g) : 0.0f;
+}
+
 // one 16-element weight chunk: fake-quantize and store its 32 bytes into the
 // swizzled tile (row n, 16-byte chunks 2j and 2j+1 of the row's 128 bytes)
 __device__ __forceinline__ void qdq_store_chunk(const uint32_t (&xw)[8], float sb, float g,
+                                                float rg, float ng, const ScaleEntry* tab,
                                                 uint8_t* tile, int n, int j) {
-  uint32_t ecode;
-  const float s = nvfp4_block_scale(sb, g, ecode);
-  uint32_t yw[8], cw[4];
-  const Divisor dv = make_divisor(s, chunk_amax(xw));
-  const IntRange r{-6.0f, 6.0f};
-  if (dv.fast) qdq_chunk_fast<F_NVFP4, false>(xw, dv, r, yw, cw);
-  else qdq_chunk<F_NVFP4, false>(xw, s, r, yw, cw);
+  const uint32_t ecode = cvt_e4m3x2(0.0f, block_quotient(sb, g, rg, ng)) & 0xFFu;
+  ScaleEntry se;
+  if (ecode < 128u) {
+    se = tab[ecode];
+  } else {  // a negative block scale: never the short path
+    se.s = __fmul_rn(dec_e4m3x2(ecode).x, g);
+    se.r = __int_as_float(0x7FC00000);
+  }
+  uint32_t aw[8], m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    aw[i] = xw[i] & 0x7FFF7FFFu;
+    m = __vmaxu2(m, aw[i]);
+  }
+  const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+  uint32_t yw[8];
+  if (__fmul_rn(amax, se.r) <= 0x1p100f) {  // make_divisor's fast test (NaN r fails)
+    const f2 R = mk2(se.r, se.r), S = mk2(se.s, se.s), NS = mk2(-se.s, -se.s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // |x| of the pair, divided (Markstein, as mdiv), rounded to E2M1, times S_hat
+      const f2 x = mk2(__uint_as_float(aw[i] << 16), __uint_as_float(aw[i] & 0xFFFF0000u));
+      const f2 q0 = mul2(x, R);
+      const f2 v = fma2(fma2(q0, NS, x), R, q0);
+      const uint32_t h = e2m1_q2(hi2(v), lo2(v));
+      const f2 y = mul2(mk2(h2f(uint16_t(h & 0xFFFFu)), h2f(uint16_t(h >> 16))), S);
+      yw[i] = pack_bf16x2(hi2(y), lo2(y)) | (xw[i] & 0x80008000u);
+    }
+  } else {
+    uint32_t cw[4];
+    qdq_chunk<F_NVFP4, false>(xw, se.s, IntRange{-6.0f, 6.0f}, yw, cw);
+  }
   const int sw = n & 7;
   uint8_t* row = tile + n * 128;
   *reinterpret_cast<uint4*>(row + (((2 * j) ^ sw) * 16)) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
@@ -130,10 +262,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* tiles_a = smem;                          // [STAGES][MT][16 KiB]
-  uint8_t* tiles_b = smem + STAGES * kStageA;        // [STAGES][16 KiB]
-  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + STAGES * (kStageA + kTileBytes));
+  uint8_t* tiles_a = smem;                     // [XS][MT][16 KiB]
+  uint8_t* tiles_b = smem + XS * kStageA;      // [WS][16 KiB]
+  GemmShared* sh = reinterpret_cast<GemmShared*>(smem + kRings);
+  ScaleEntry* stab = reinterpret_cast<ScaleEntry*>(smem + kRings + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = int(cluster_ctarank()), ccount = int(cluster_nctarank());  // 1 or kCN
+  const uint16_t cmask = uint16_t((1u << ccount) - 1u);
 
   if (warp == 0) {
     int e, mt;
@@ -142,9 +277,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       sh->expert = e;
       sh->mtile = mt;
       sh->abort = 0;
-      for (int s = 0; s < STAGES; ++s) {
-        mbar_init(&sh->full[s], 1 + kProducerThreads / 32);
-        mbar_init(&sh->empty[s], 1);
+      for (int s = 0; s < XS; ++s) {
+        mbar_init(&sh->full_x[s], 1);
+        mbar_init(&sh->empty_x[s], ccount);  // one commit from each CTA of the cluster
+      }
+      for (int s = 0; s < WS; ++s) {
+        mbar_init(&sh->full_w[s], kProducerThreads / 32);
+        mbar_init(&sh->empty_w[s], 1);
       }
       mbar_init(&sh->accum, 1);
       fence_barrier_init();
@@ -153,9 +292,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
   const int e = sh->expert;
-  if (e < 0) return;  // grid rows beyond the last tile: no work, nothing allocated
+  // grid rows beyond the last tile: no work, nothing allocated (a cluster's
+  // CTAs share the grid row, so they leave together)
+  if (e < 0) return;
+  cluster_sync();  // the peers' barriers are initialised before any multicast
   const int mt = sh->mtile;
-  if (warp == 1) tmem_alloc(&sh->tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&sh->tmem, kTmemCols);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -170,59 +312,80 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nt = blockIdx.x;
   const int KT = int(a.K / BK);
 
-  if (warp == 0) {
+  const bool producer = warp >= 2 && warp != kTmaWarp && warp != 9;
+  if (warp == kTmaWarp) {
     // ---- TMA producer ----
     if (lane == 0) {
       int issued = 0;
       for (int kt = 0; kt < KT && !aborted(sh); ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES && !mbar_wait(&sh->empty[s], ((kt / STAGES) & 1) ^ 1)) {
+        const int s = kt % XS;
+        if (kt >= XS && !mbar_wait(&sh->empty_x[s], ((kt / XS) & 1) ^ 1)) {
           set_abort(sh);
           break;
         }
-        mbar_arrive_expect_tx(&sh->full[s], kTileBytes * ntiles);
-        for (int i = 0; i < ntiles; ++i)
-          tma_load_2d(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full[s], kt * BK,
-                      int32_t(row0 + i * BM));
+        mbar_arrive_expect_tx(&sh->full_x[s], kTileBytes * ntiles);  // every CTA's tiles
+        for (int i = crank; i < ntiles; i += ccount) {
+          if (ccount > 1)
+            tma_load_2d_mc(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full_x[s], kt * BK,
+                           int32_t(row0 + i * BM), cmask);
+          else
+            tma_load_2d(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full_x[s], kt * BK,
+                        int32_t(row0 + i * BM));
+        }
         ++issued;
       }
       if (aborted(sh)) {
         // let the copies already issued land before the CTA's memory goes away
-        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt)
-          mbar_wait(&sh->full[kt % STAGES], (kt / STAGES) & 1);
+        for (int kt = (issued > XS ? issued - XS : 0); kt < issued; ++kt)
+          mbar_wait(&sh->full_x[kt % XS], (kt / XS) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issuer ----
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      // descriptors of stage 0; a stage, row tile or K-slice offset adds to
+      // the start-address field (addresses stay below 256 KiB: no carry)
+      const uint64_t da0 = smem_desc_sw128(smem_u32(tiles_a));
+      const uint64_t db0 = smem_desc_sw128(smem_u32(tiles_b));
       bool ok = true;
       for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % STAGES;
-        if (aborted(sh) || !mbar_wait(&sh->full[s], (kt / STAGES) & 1)) {
+        const int s = kt % XS, sw = kt % WS;
+        if (aborted(sh) || !mbar_wait(&sh->full_x[s], (kt / XS) & 1) ||
+            !mbar_wait(&sh->full_w[sw], (kt / WS) & 1)) {
           set_abort(sh);
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t sa = smem_u32(tiles_a + s * kStageA);
-        const uint32_t sb = smem_u32(tiles_b + s * kTileBytes);
+        const uint64_t da = da0 + ((s * kStageA) >> 4), db = db0 + ((sw * kTileBytes) >> 4);
+        // unrolled to MT with a guard: a loop bounded by the run-time tile
+        // count issues the MMAs markedly slower
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t db = smem_desc_sw128(sb + kk * 32);
-          for (int i = 0; i < ntiles; ++i)
-            tc_mma_f16(tmem + uint32_t(i * BN), smem_desc_sw128(sa + i * kTileBytes + kk * 32), db,
-                       idesc, (kt | kk) != 0);
+#pragma unroll
+          for (int i = 0; i < MT; ++i)
+            if (i < ntiles)
+              tc_mma_f16(tmem + uint32_t(i * BN), da + ((i * kTileBytes + kk * 32) >> 4),
+                         db + ((kk * 32) >> 4), idesc, (kt | kk) != 0);
         }
-        tc_commit(&sh->empty[s]);
+        if (ccount > 1) tc_commit_mc(&sh->empty_x[s], cmask);
+        else tc_commit(&sh->empty_x[s]);
+        tc_commit(&sh->empty_w[sw]);
       }
       tc_commit(&sh->accum);
       if (!ok) mbar_wait(&sh->accum, 0);  // drain the MMAs already issued
     }
-  } else {
+  } else if (producer) {
     // ---- weight producers (fake-quant into shared memory) ----
-    const int pt = threadIdx.x - 64;  // 0..255
+    const int pw = warp - 2 - (warp > kTmaWarp ? 1 : 0) - (warp > 9 ? 1 : 0);  // 0..7
+    const int pt = pw * 32 + lane;                                              // 0..255
     const float g = __ldg(a.tscale + e);
+    const bool gfast = (g >= 0x1p-64f) && (g <= 0x1p64f);
+    const float rg = gfast ? __frcp_rn(g) : __int_as_float(0x7FC00000), ng = -g;
+    if (pt < 128) stab[pt] = scale_entry(uint32_t(pt), g);
+    // the eight producer warps only: named barrier 1
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducerThreads) : "memory");
     const int64_t kb = a.K / 16;
     const uint8_t* wrow = a.w + (size_t(e) * a.N + size_t(nt) * BN) * size_t(a.K) * 2;
     const float* srow = a.scale + (size_t(e) * a.N + size_t(nt) * BN) * size_t(kb);
@@ -242,7 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       sbv[i] = __ldg(srow + size_t(n_[i]) * kb + j_[i]);
     }
     for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % STAGES;
+      const int s = kt % WS;
       uint32_t nx[2][8];
       float nsb[2];
       const bool more = kt + 1 < KT;
@@ -257,7 +420,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       if (lane == 0) {
         ok = !aborted(sh);
-        if (ok && kt >= STAGES) ok = mbar_wait(&sh->empty[s], ((kt / STAGES) & 1) ^ 1);
+        if (ok && kt >= WS) ok = mbar_wait(&sh->empty_w[s], ((kt / WS) & 1) ^ 1);
         if (!ok) set_abort(sh);
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -265,10 +428,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       uint8_t* tile = tiles_b + s * kTileBytes;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) qdq_store_chunk(xw[i], sbv[i], g, tile, n_[i], j_[i]);
+      for (int i = 0; i < 2; ++i) qdq_store_chunk(xw[i], sbv[i], g, rg, ng, stab, tile, n_[i], j_[i]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->full[s]);
+      if (lane == 0) mbar_arrive(&sh->full_w[s]);
       if (more) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -278,6 +441,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
+  }
+  if (warp >= 4) {
     // ---- epilogue: TMEM lane quarter = warp % 4, two warps per quarter ----
     {
       bool ok = true;
@@ -290,34 +455,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok) {
         tc_fence_after_sync();
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;  // 0 for warps 2-5, 1 for warps 6-9
+        const int half = (warp - 4) >> 2;  // 0 for warps 4-7, 1 for warps 8-11
+        // staging for 32 rows x 128 columns of BF16 (8 KiB per warp) in the
+        // X ring, idle once the accumulators are complete; 16-byte unit c of
+        // row r sits at unit c ^ (r % 16), so both the row-wise writes and the
+        // column-wise reads below are free of bank conflicts
+        uint8_t* stage = tiles_a + (warp - 4) * (32 * BN * 2);
 #pragma unroll 1
-        for (int p = half; p < ntiles * (BN / 32); p += 2) {
-          const int i = p / (BN / 32), cc = p % (BN / 32);
-          const int r = i * BM + q * 32 + lane;  // row within the group
-          uint8_t* yrow = a.y + (size_t(row0 + r) * size_t(a.N) + size_t(nt) * BN) * 2;
-          uint32_t v[32];
-          tc_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(i * BN + cc * 32), v);
-          tc_wait_ld();
-          if (r < rows_valid) {
-            uint32_t o[16];
+        for (int i = half; i < ntiles; i += 2) {
+          const int rb = i * BM + q * 32;  // first row of this warp's block within the group
+          if (rb >= rows_valid) break;
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(i * BN + cc * 32), v);
+            tc_wait_ld();
+            uint8_t* srow = stage + lane * (BN * 2);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              o[i] = pack_bf16x2(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[2 * i]));
-            uint4* dst = reinterpret_cast<uint4*>(yrow + cc * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            for (int u = 0; u < 4; ++u) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[8 * u + 1]), __uint_as_float(v[8 * u]));
+              o.y = pack_bf16x2(__uint_as_float(v[8 * u + 3]), __uint_as_float(v[8 * u + 2]));
+              o.z = pack_bf16x2(__uint_as_float(v[8 * u + 5]), __uint_as_float(v[8 * u + 4]));
+              o.w = pack_bf16x2(__uint_as_float(v[8 * u + 7]), __uint_as_float(v[8 * u + 6]));
+              *reinterpret_cast<uint4*>(srow + (((cc * 4 + u) ^ (lane & 15)) * 16)) = o;
+            }
           }
+          __syncwarp();
+          // two rows of 256 bytes per instruction
+#pragma unroll 4
+          for (int t = 0; t < 16; ++t) {
+            const int rr = 2 * t + (lane >> 4), c = lane & 15;
+            const uint4 o = *reinterpret_cast<const uint4*>(stage + rr * (BN * 2) + ((c ^ (rr & 15)) * 16));
+            if (rb + rr < rows_valid)
+              *reinterpret_cast<uint4*>(a.y + (size_t(row0 + rb + rr) * size_t(a.N) + size_t(nt) * BN) * 2 +
+                                        c * 16) = o;
+          }
+          __syncwarp();
         }
       }
     }
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // no CTA leaves while a peer's multicast loads or commits may still reach it
+  cluster_sync();
   if (threadIdx.x == 0 && aborted(sh) && a.err) atomicExch(a.err, 1);
 }
 
@@ -404,10 +590,22 @@ extern "C" aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_off
   a.N = N;
   a.K = K;
   a.total_m = total_m;
-  dim3 grid(unsigned(N / BN), unsigned(slots), 1);
-  grouped_qdq_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, static_cast<cudaStream_t>(stream)>>>(tm,
-                                                                                                a);
-  return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
+  // clusters of kCN column tiles when the column tiles divide evenly, else single CTAs
+  const unsigned ntn = unsigned(N / BN);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (ntn % kCN == 0) ? kCN : 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ntn, unsigned(slots), 1);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_qdq_gemm_kernel, tm, a) == cudaSuccess ? AQFQ_OK
+                                                                                : AQFQ_ERR_CUDA;
 }
 
 extern "C" aqfq_status aqfq_selftest_wait_timeout(int32_t* flag, uint32_t polls, void* stream) {

@@ -74,6 +74,48 @@ def test_gemm_random_within_bound(E, N, K, sizes):
     assert np.median(rel) < 2.0 ** -8
 
 
+def _e4m3_midpoints():
+    """Midpoints between consecutive positive finite E4M3 values, and the
+    saturation threshold halfway between 448 and the next step (480)."""
+    vals = []
+    for c in range(0x7F):  # 0x7F is NaN
+        e, m = c >> 3, c & 7
+        vals.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    vals = np.array(sorted(set(vals)))
+    return np.concatenate([(vals[1:] + vals[:-1]) / 2, [464.0]])
+
+
+def test_gemm_block_scale_quotient_at_e4m3_midpoints():
+    """Block scales whose quotient S_b / g lies within a few binary32 ulps of
+    an E4M3 rounding midpoint (where a quotient off by one ulp changes the
+    block's code), plus zero, subnormal, tiny and huge quotients that leave the
+    kernel's short division path: one-hot rows make Y = w_hat^T bit for bit."""
+    E, N, K = 2, 128, 1024
+    rng = np.random.default_rng(77)
+    g = (rng.uniform(1.0, 2.0, E) * 3e-5).astype(np.float32)
+    mids = _e4m3_midpoints()
+    deltas = np.array([0.0, 2.0 ** -24, -2.0 ** -24, 2.0 ** -23, -2.0 ** -23, 3 * 2.0 ** -24, -3 * 2.0 ** -24])
+    nb = N * K // 16
+    s = np.empty((E, nb), dtype=np.float32)
+    for e in range(E):
+        combo = rng.permutation(np.array([(m, d) for m in mids for d in deltas]))
+        reps = np.resize(combo, (nb, 2))
+        s[e] = (reps[:, 0] * float(g[e]) * (1.0 + reps[:, 1])).astype(np.float32)
+        special = np.array([0.0, 1e-40, float(g[e]) * 2.0 ** -35, float(g[e]) * 2.0 ** -29,
+                            float(g[e]) * 2.0 ** 101, float(g[e]) * 500.0, 1e30], dtype=np.float32)
+        s[e, rng.choice(nb, special.size * 8, replace=False)] = np.tile(special, 8)
+    w = synth.normal_bf16((E, N, K), 0.02, 78)
+    M = E * K
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    x[torch.arange(M), torch.arange(M) % K] = 1.0
+    off = torch.tensor([0, K, 2 * K], dtype=torch.int32)
+    st, gt = torch.from_numpy(s.reshape(-1)), torch.from_numpy(g)
+    y = _run(x, off, w, st, gt)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), st.numpy(), gt.numpy())
+    yb, rb = bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16))
+    assert np.array_equal(yb, rb), f"{np.count_nonzero(yb != rb)} of {yb.size} differ"
+
+
 def test_gemm_argument_checks():
     d = dev()
     x = torch.zeros((16, 64), dtype=torch.bfloat16, device=d)
