@@ -908,7 +908,8 @@ __global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(cons
   cluster_sync();
 }
 
-// number of positions whose label lies in [0, V); clears the error word
+// number of positions whose label lies in [0, V); clears the error word and
+// the mean kernel's ticket
 __global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* head) {
   __shared__ int part[32];
   int c = 0;
@@ -922,19 +923,29 @@ __global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int
     for (int k = 0; k < int(blockDim.x >> 5); ++k) s += part[k];
     head[0] = s;
     head[1] = 0;
+    head[2] = 0;  // the mean kernel's ticket
   }
 }
 
 // Per position: forward / reverse KL = tau^2 x the sum of the slices' sums
 // (rank order), the loss of the selected type, written to token_loss; then
 // losses[k] = the sums over the valid positions / their number (double
-// accumulation, fixed order); NaN if a copy wait of the loss kernel timed out.
-__global__ void kd_mean_kernel(const float* part, const float* rowx, const int32_t* labels,
-                               const int32_t* head, int64_t T, int64_t V, int type, float tau2,
-                               float* token_loss, float* losses) {
-  __shared__ double acc[32][3];
+// accumulation in a fixed order: block b sums positions [b c, b c + c) by a
+// fixed pattern, the last block to finish adds the blocks' sums in block
+// order); NaN if a copy wait of the loss kernel timed out.
+constexpr int kMeanBlocks = 32;
+__global__ void __launch_bounds__(256) kd_mean_kernel(const float* part, const float* rowx,
+                                                      const int32_t* labels, int32_t* head,
+                                                      double* bsum, int64_t T, int64_t V,
+                                                      int type, float tau2, float* token_loss,
+                                                      float* losses) {
+  __shared__ double acc[8][3];
+  __shared__ int last;
+  const int64_t c = (T + gridDim.x - 1) / gridDim.x;
+  const int64_t i0 = int64_t(blockIdx.x) * c;
+  const int64_t i1 = i0 + c < T ? i0 + c : T;
   double s[3] = {0.0, 0.0, 0.0};
-  for (int64_t i = threadIdx.x; i < T; i += blockDim.x) {
+  for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     const int32_t l = labels[i];
     float loss = 0.0f;
     if (l >= 0 && int64_t(l) < V) {
@@ -967,6 +978,17 @@ __global__ void kd_mean_kernel(const float* part, const float* rowx, const int32
   if (threadIdx.x < 3) {
     double t = 0.0;
     for (int w = 0; w < int(blockDim.x >> 5); ++w) t += acc[w][threadIdx.x];
+    bsum[blockIdx.x * 3 + threadIdx.x] = t;
+    __threadfence();  // each writer's sum is visible device-wide before the ticket
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&head[2], 1) == int(gridDim.x) - 1;
+  __syncthreads();
+  if (last && threadIdx.x < 3) {
+    __threadfence();
+    double t = 0.0;
+    for (int b = 0; b < int(gridDim.x); ++b)
+      t += *reinterpret_cast<volatile const double*>(&bsum[b * 3 + threadIdx.x]);
     const int n = T > 0 ? head[0] : 0;
     float r = n > 0 ? float(t / double(n)) : 0.0f;
     if (T > 0 && head[1] != 0) r = __int_as_float(0x7FC00000);
@@ -983,9 +1005,12 @@ namespace {
 
 using namespace aqfq;
 
-// workspace: [0, 256) int32 valid count and error word; then part [T, kCl, 2]
-// and rowx [T, 2] floats, each starting on a 256-byte boundary
-constexpr size_t kWsHead = 256;
+// workspace: [0, 256) int32 valid count, error word and the mean kernel's
+// ticket; [256, 1024) the mean kernel's per-block double sums; then part
+// [T, kCl, 2] and rowx [T, 2] floats, each starting on a 256-byte boundary
+constexpr size_t kWsHead = 1024;
+constexpr size_t kWsBsum = 256;
+static_assert(kWsBsum + kMeanBlocks * 3 * sizeof(double) <= kWsHead, "block sums fit the head");
 size_t ws_part_bytes(int64_t T) { return (size_t(T) * kCl * 8 + 255) / 256 * 256; }
 
 size_t kd_smem_bytes(int32_t S, bool topk) {
@@ -1101,7 +1126,8 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
                    : launch_kd<false, false, false>(a, smem, st);
     if (e != cudaSuccess) return AQFQ_ERR_CUDA;
   }
-  kd_mean_kernel<<<1, 1024, 0, st>>>(part, rowx, labels, head, T, V, kd_type,
-                                     temperature * temperature, token_loss, losses);
+  double* bsum = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) + kWsBsum);
+  kd_mean_kernel<<<kMeanBlocks, 256, 0, st>>>(part, rowx, labels, head, bsum, T, V, kd_type,
+                                              temperature * temperature, token_loss, losses);
   return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
 }

@@ -188,8 +188,8 @@ def test_kd_loss_host_checks(L):
     assert kd(L, s=A + 8) == ALIGN
     assert kd(L, ds=6 * A + 4) == ALIGN
     assert kd(L, tl=6 * A + 2) == ALIGN
-    assert aqfq.aqfq_kd_workspace_bytes(0) == 256
-    assert aqfq.aqfq_kd_workspace_bytes(4096) >= 256 + 12 * 4096
+    assert aqfq.aqfq_kd_workspace_bytes(0) == 1024
+    assert aqfq.aqfq_kd_workspace_bytes(4096) >= 1024 + 12 * 4096
 
 
 def test_selftest_wait_timeout_host_checks(L):
