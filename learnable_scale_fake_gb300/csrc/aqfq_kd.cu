@@ -104,7 +104,7 @@ struct __align__(16) KdShared {
 struct __align__(16) TopkShared {
   uint32_t hist2[16];       // low nibble of the keys in the threshold bin
   uint32_t h2all[kCl][16];  // hist2 of every rank
-  uint32_t bins[32];        // cluster-wide counts of 32 histogram bins
+  uint32_t bins[8 * (kThr / kCl)];  // cluster-wide counts of one search step's bins
 };
 
 // ---------------------------------------------------------------------------
@@ -139,6 +139,15 @@ __device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank
 __device__ __forceinline__ float ld_remote_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+// 16 bytes (four words) from a 16-byte aligned shared::cluster address
+__device__ __forceinline__ uint4 ld_remote_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
   return v;
 }
 __device__ __forceinline__ uint32_t ld_remote_u32(uint32_t a) {
@@ -381,35 +390,65 @@ __device__ __forceinline__ int block_scan(int v, int& total, KdShared* sh) {
 // cluster-wide count of a 4096-bin histogram (16-bit counters, bin b in half
 // b & 1 of word b >> 1) reaches K, and the count above
 // that bin.  Returns false (bin 0, the whole count) when the histogram holds
-// fewer than K.  All threads call it.  Each step covers 32 bins: thread t
-// loads bin t / 16 of the step from rank t % 16 (one remote load each).
+// fewer than K.  All threads call it.  A step covers 8 * kThr / kCl bins (256
+// with 256 threads and 8 ranks) in aligned blocks of 8: thread t loads block
+// t / kCl of the step from rank t % kCl (one 16-byte remote load), the kCl
+// threads of a block add their counts, and one warp scans the step's bins
+// from the top.  Steps start at the top of `top`'s block (bins above `top`
+// are empty).
 __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int K, int& bin,
                                               int& above, KdShared* sh, TopkShared* tk) {
-  static_assert(kThr >= 32 * kCl && kCl <= 32, "one remote load per thread per 32-bin step");
+  constexpr int kBlocks = kThr / kCl;  // 8-bin blocks per step
+  constexpr int kStep = 8 * kBlocks;
+  static_assert(kThr % kCl == 0 && 32 % kCl == 0, "the ranks of a block share a warp");
+  static_assert(kStep % 256 == 0 && kStep <= 1024, "the scanning warp takes kStep / 32 bins per lane");
+  constexpr int kPer = kStep / 32;  // bins per lane of the scanning warp
   const int tid = threadIdx.x, j = tid / kCl, r = tid % kCl;
-  const bool part = tid < 32 * kCl;
   int base = 0;
-  for (int b0 = top; b0 >= 0; b0 -= 32) {
-    const int b = b0 - j;
-    uint32_t c = (part && b >= 0)
-                     ? (ld_remote_u32(remote_addr(hist + (b >> 1), r)) >> ((b & 1) * 16)) & 0xFFFFu
-                     : 0u;
+  for (int hi = top | 7; hi >= 0; hi -= kStep) {
+    const int bh = hi - 8 * j;  // this block: bins [bh - 7, bh]; bh % 8 == 7
+    uint32_t c[8];              // c[i]: bin bh - i
+    {
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (bh >= 0) w = ld_remote_v4(remote_addr(hist + ((bh - 7) >> 1), uint32_t(r)));
+      const uint32_t q[4] = {w.x, w.y, w.z, w.w};  // word m holds bins bh-7+2m (low), bh-6+2m (high)
 #pragma unroll
-    for (int d = kCl / 2; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
-    if (part && r == 0) tk->bins[j] = c;
+      for (int i = 0; i < 8; ++i) c[i] = (q[(7 - i) >> 1] >> (((7 - i) & 1) * 16)) & 0xFFFFu;
+    }
+#pragma unroll
+    for (int d = kCl / 2; d >= 1; d >>= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] += __shfl_xor_sync(0xFFFFFFFFu, c[i], d);
+    if (r == 0)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tk->bins[8 * j + i] = c[i];  // step index 8 j + i = bin hi - (8 j + i)
     __syncthreads();
-    if (tid < 32) {  // one warp scans the 32 bins from the top
-      const int cj = int(tk->bins[tid]);
-      int x = cj;
+    if (tid < 32) {  // lane l: step indices [kPer l, kPer l + kPer), from the top down
+      uint32_t v[kPer];
+      int cl = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        v[i] = tk->bins[kPer * tid + i];
+        cl += int(v[i]);
+      }
+      int x = cl;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
         if (tid >= d) x += y;
       }
       const int incl = base + x;
-      if (incl - cj < K && incl >= K) {
-        sh->sel[6] = b0 - tid;
-        sh->sel[7] = incl - cj;
+      if (incl - cl < K && incl >= K) {  // the crossing lies in this lane's bins
+        int run = incl - cl;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          if (run + int(v[i]) >= K) {
+            sh->sel[6] = hi - (kPer * tid + i);
+            sh->sel[7] = run;
+            break;
+          }
+          run += int(v[i]);
+        }
       }
       if (tid == 31) sh->sel[1] = incl;  // running total after this step
     }
