@@ -64,6 +64,10 @@ constexpr int kNbuf = AQFQ_KD_NBUF;   // slice buffers per CTA
 #define AQFQ_KD_THREADS 256
 #endif
 constexpr int kThr = AQFQ_KD_THREADS;  // threads per CTA
+#ifndef AQFQ_KD_MINB
+#define AQFQ_KD_MINB (AQFQ_KD_THREADS <= 256 ? 3 : 2)
+#endif
+constexpr int kMinBlocks = AQFQ_KD_MINB;  // CTAs per SM the register budget is sized for
 constexpr int kWarps = kThr / 32;
 constexpr int kHist1 = 4096;    // bins: the top 12 bits of the 16-bit teacher key
 constexpr int kHistWords = kHist1 / 2;  // two 16-bit counters per word (a slice has < 2^16 elements)
@@ -401,7 +405,7 @@ __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int
   constexpr int kBlocks = kThr / kCl;  // 8-bin blocks per step
   constexpr int kStep = 8 * kBlocks;
   static_assert(kThr % kCl == 0 && 32 % kCl == 0, "the ranks of a block share a warp");
-  static_assert(kStep % 256 == 0 && kStep <= 1024, "the scanning warp takes kStep / 32 bins per lane");
+  static_assert(kStep % 32 == 0 && kStep <= 1024, "the scanning warp takes kStep / 32 bins per lane");
   constexpr int kPer = kStep / 32;  // bins per lane of the scanning warp
   const int tid = threadIdx.x, j = tid / kCl, r = tid % kCl;
   int base = 0;
@@ -504,7 +508,7 @@ __device__ __forceinline__ void ordered_scan(const uint16_t* tsl, const uint16_t
 //          2^(x_s - m) (x_s - x_t) for the reverse KL that centres it
 //   MSE    mean squared error loss and gradient
 template <bool TOPK, bool RGRAD, bool MSE>
-__global__ void __launch_bounds__(kThr, kThr <= 256 ? 3 : 2) kd_loss_kernel(const KdArgs a) {
+__global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs a) {
   extern __shared__ __align__(16) uint8_t kd_smem[];
   KdShared* sh = reinterpret_cast<KdShared*>(kd_smem);
   const int nvb = TOPK ? (a.S / 8 + 7) / 8 * 8 : 0;  // vector slots, padded to 16 bytes
