@@ -149,3 +149,44 @@ def test_grouped_e2e_pipeline_matches_device_step():
         torch.cuda.synchronize()
         for k, v in ref.items():
             assert torch.equal(hout[k].view(torch.uint8), v.cpu().view(torch.uint8)), k
+
+
+def test_fused_gemm_full_size_sampled():
+    """The fused fake-quant + grouped GEMM on the bench's workload (65536 routed
+    rows, W [128, 1536, 2048], uneven routing): outputs at every expert's first
+    and last row, on both sides of every 512-row group boundary and at random
+    rows, three columns each, recomputed by the oracle from the one X row and
+    the weight rows they need; within the same bound as the small cases
+    (|y - ref| <= 2^-8 |ref| + K 2^-24 sum_k |x w_hat|)."""
+    d = dev()
+    wl = workloads.grouped_nvfp4_gemm(d)
+    _run(wl)
+    assert int(wl.err.item()) == 0, "a pipeline wait timed out"
+    x, off, w = wl.inputs["x"], wl.inputs["m_offsets"], wl.inputs["w"]
+    s, g, y = wl.inputs["scale"], wl.inputs["tscale"], wl.outputs["y"]
+    E, N, K = w.shape
+    offs = off.cpu().numpy().astype(np.int64)
+    rows = set()
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi > lo:
+            rows.update((lo, hi - 1))
+        for b in range(lo + 512, hi, 512):  # a group boundary: last row before, first after
+            rows.update((b - 1, b))
+    rng = np.random.default_rng(5)
+    rows.update(int(r) for r in rng.integers(0, x.shape[0], 64))
+    rows = np.array(sorted(rows), dtype=np.int64)
+    assert rows.size > 3 * E  # the routing is uneven: many experts span two groups
+    cols = rng.integers(0, N, (rows.size, 3))
+    cols[0, 0], cols[-1, -1] = 0, N - 1
+    xr = bits(x[torch.from_numpy(rows).to(d)].cpu())
+    sv = s.view(E, N, K // 16)
+    gh = _f32(g)
+    for i, m in enumerate(rows):
+        e = int(np.searchsorted(offs, m, side="right") - 1)
+        c = torch.from_numpy(cols[i]).to(d)
+        ref, absref = O.grouped_qdq_gemm(xr[i:i + 1], [0, 1], bits(w[e, c].cpu())[None],
+                                         _f32(sv[e, c]).reshape(-1), gh[e:e + 1])
+        got = y[int(m), c].float().cpu().numpy().astype(np.float64)
+        tol = 2.0 ** -8 * np.abs(ref[0]) + K * 2.0 ** -24 * absref[0]
+        assert np.all(np.abs(got - ref[0]) <= tol), (int(m), e, cols[i], got, ref[0])
