@@ -29,8 +29,9 @@
 // The CTAs of a cluster (kCN column tiles of the same row group) read the same
 // X tiles: each loads every kCN-th tile and multicasts it to all of them, and
 // every CTA's MMA commit releases an X stage in all of them (an X stage is
-// refilled only once every CTA has consumed it).  This divides the L2 -> SM
-// traffic for X, which otherwise paces the loads, by kCN.
+// refilled only once every CTA has consumed it).  This divides the L2 reads
+// for X by kCN; the loads stay paced by each SM's intake of operand bytes,
+// which multicast does not change.
 // Every wait is bounded; on a timeout the CTA drains what it issued, frees
 // its tensor memory, raises the caller's error flag and returns.
 #include <cuda.h>
