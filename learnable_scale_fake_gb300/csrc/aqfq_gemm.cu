@@ -163,8 +163,9 @@ __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int sl
 // ---- weight fake-quant in the producers ------------------------------------
 // The same values as aqfq_qdq_fwd's NVFP4 chunk arithmetic, arranged for
 // issue throughput (the producers' instruction count paces the main loop):
-// the expert's 256 possible block scales S_hat = RN(dec(e) g) and their
-// reciprocals come from a table built once per CTA, the block-scale quotient
+// the block scales S_hat = RN(dec(e) g) of the 128 non-negative E4M3 codes and
+// their reciprocals come from a table built once per CTA (a negative code takes
+// the IEEE path), the block-scale quotient
 // S_b / g uses Markstein's correction with RN(1/g), and the per-element
 // division and dequantisation run as packed f32x2 operations (IEEE
 // round-to-nearest per lane, so every result is the scalar path's).
@@ -304,11 +305,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem;
 
-  // rows [row0, row0 + rows_valid) of this expert, MT tiles at most
-  const int64_t row0 = int64_t(a.off[e]) + int64_t(mt) * MT * BM;
-  int64_t rows_valid = int64_t(a.off[e + 1]) - row0;
+  // the expert's rows [lo, hi), offsets clamped to [0, total_m] as find_tile
+  // counts them; this group: rows [row0, row0 + rows_valid), MT tiles at most
+  // (an even spread of the tiles over the groups measured 1.8 % slower)
+  int64_t lo = a.off[e], hi = a.off[e + 1];
+  if (lo < 0) lo = 0;
+  if (hi > a.total_m) hi = a.total_m;
+  const int64_t row0 = lo + int64_t(mt) * MT * BM;
+  int64_t rows_valid = hi - row0;
   if (rows_valid > MT * BM) rows_valid = MT * BM;
-  if (row0 + rows_valid > a.total_m) rows_valid = a.total_m - row0;
   const int ntiles = int((rows_valid + BM - 1) / BM);  // 1..MT
   const int nt = blockIdx.x;
   const int KT = int(a.K / BK);

@@ -116,6 +116,16 @@ def test_gemm_block_scale_quotient_at_e4m3_midpoints():
     assert np.array_equal(yb, rb), f"{np.count_nonzero(yb != rb)} of {yb.size} differ"
 
 
+def test_gemm_offsets_clamped_to_rows():
+    """Offsets below 0 or beyond total_m are clamped to [0, total_m]: the kernel
+    computes the clamped experts and touches no row outside Y."""
+    x, _, w, s, g = _inputs(2, 128, 128, [130, 70], 240, onehot=True)
+    off = torch.tensor([-7, 130, 260], dtype=torch.int32)
+    y = _run(x, off, w, s, g)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), [0, 130, 200], bits(w), s.numpy(), g.numpy())
+    assert np.array_equal(bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16)))
+
+
 def test_gemm_argument_checks():
     d = dev()
     x = torch.zeros((16, 64), dtype=torch.bfloat16, device=d)
