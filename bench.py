@@ -517,10 +517,20 @@ def main():
 
         k, _, desc = oracle_pick(args.workload, wl.inputs, target_s=20.0)
         nbytes, elems, secs = oracle_run(args.workload, wl.inputs, k)
+        threads = oracle.num_threads()
         cpu = {"value": round(nbytes / secs / scale_unit, 6), "unit": "TFLOP/s" if flops_kind else "GB/s",
-               "cores": oracle.num_threads(), "kind": "oracle",
+               "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2),
                "gelem_per_s": round(elems / secs / 1e9, 5)}
+        # the same oracle on one thread, on a smaller sample
+        oracle.set_num_threads(1)
+        try:
+            k1, _, desc1 = oracle_pick(args.workload, wl.inputs, target_s=6.0)
+            nb1, _, s1 = oracle_run(args.workload, wl.inputs, k1)
+        finally:
+            oracle.set_num_threads(threads)
+        cpu["single_thread"] = {"value": round(nb1 / s1 / scale_unit, 6), "sample": desc1,
+                                "seconds": round(s1, 2)}
 
     if rank == 0:
         metric = metric_name(args.workload, flops_kind)

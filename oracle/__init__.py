@@ -89,6 +89,8 @@ def lib():
             L.orc_scale_init.restype = ctypes.c_int
             L.orc_scale_init.argtypes = [ctypes.POINTER(Spec), P, i64, i64, i64, P, P]
             L.orc_num_threads.restype = ctypes.c_int
+            L.orc_set_num_threads.restype = None
+            L.orc_set_num_threads.argtypes = [ctypes.c_int]
             L.orc_kd_loss.restype = ctypes.c_int
             L.orc_kd_loss.argtypes = [ctypes.c_int, P, P, P, i64, i64, ctypes.c_int32,
                                       ctypes.c_double, ctypes.c_double, P, P, P, P, P, P]
@@ -106,6 +108,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (n >= 1)."""
+    lib().orc_set_num_threads(int(n))
 
 
 # ---- primitives -----------------------------------------------------------------

@@ -26,6 +26,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* threads for the parallel loops that follow (timing a single-thread baseline) */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : 1);
+#else
+  (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------- */
 /* binary32 and bf16                                                          */
 /* ------------------------------------------------------------------------- */

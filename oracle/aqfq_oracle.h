@@ -90,6 +90,7 @@ int orc_scale_init(const orc_spec* sp, const uint16_t* x, int64_t batch, int64_t
                    int64_t K, float* scale, float* tensor_scale);
 
 int orc_num_threads(void);
+void orc_set_num_threads(int n);
 
 /* ---- distillation losses (kd_oracle.c) ----
  * kd_type: 0 kl (forward KL), 1 rkl (reverse KL), 2 cakld, 3 mse.
