@@ -50,6 +50,7 @@ def parse():
                     help="kd_cakld / kd_topk only: number of positions (small profiling case)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay leg")
     return ap.parse_args()
 
 
@@ -486,6 +487,41 @@ def main():
         unfused = {"op": rop.name, "ms": round(rms, 4),
                    "value": round(rop.bytes / (rms * 1e-3) / scale_unit, 1)}
 
+    # ---- the same step launched as one CUDA graph (beside the eager timed
+    # region: timing events cannot sit inside a captured graph, so per-op times
+    # and the roofline come from the eager region above) ----
+    graph = None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                wl.step(stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            torch.cuda.synchronize()
+            gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for k in range(args.steps):
+                    if flush is not None:
+                        flush.fill_(k & 0xFF)
+                    gev[k][0].record(stream)
+                    g.replay()
+                    gev[k][1].record(stream)
+            torch.cuda.synchronize()
+            gms = sum(a.elapsed_time(b) for a, b in gev) / args.steps
+            gms = max_over_ranks(gms, dist, device)
+            graph = {"ms_per_step": round(gms, 4),
+                     "value": round(world * bytes_step / (gms * 1e-3) / scale_unit, 1),
+                     "steps": args.steps, "timing": "CUDA events around each replay"}
+            del g
+        except Exception as ex:  # a step that cannot be captured: report why
+            graph = {"unavailable": f"{type(ex).__name__}: {ex}"[:200]}
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -549,6 +585,7 @@ def main():
                                      round(100 * value / world / NOMINAL_HBM_GBS, 1)),
             "per_op_ms": {op.name: round(op_ms[i], 4) for i, op in enumerate(wl.ops)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "unfused_path": unfused,
+            "graph": graph,
             "gpu_launches": args.steps * sum(op.launches for op in wl.ops),
             "clocks": clk,
         }
