@@ -492,6 +492,9 @@ def main():
     # and the roofline come from the eager region above) ----
     graph = None
     if not args.no_graph:
+        # every rank reaches the same collectives whether or not its capture
+        # works; a failure anywhere shows as +inf in the max over ranks
+        g, why = None, None
         try:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -500,11 +503,15 @@ def main():
                 for _ in range(3):
                     g.replay()
             torch.cuda.synchronize()
+        except Exception as ex:  # a step that cannot be captured: report why
+            g, why = None, f"{type(ex).__name__}: {ex}"[:200]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        gms = float("inf")
+        if g is not None:
             gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-            if dist is not None:
-                dist.barrier()
-            torch.cuda.synchronize()
             with torch.cuda.stream(stream):
                 for k in range(args.steps):
                     if flush is not None:
@@ -514,13 +521,14 @@ def main():
                     gev[k][1].record(stream)
             torch.cuda.synchronize()
             gms = sum(a.elapsed_time(b) for a, b in gev) / args.steps
-            gms = max_over_ranks(gms, dist, device)
+            del g
+        gms = max_over_ranks(gms, dist, device)
+        if gms != float("inf"):
             graph = {"ms_per_step": round(gms, 4),
                      "value": round(world * bytes_step / (gms * 1e-3) / scale_unit, 1),
                      "steps": args.steps, "timing": "CUDA events around each replay"}
-            del g
-        except Exception as ex:  # a step that cannot be captured: report why
-            graph = {"unavailable": f"{type(ex).__name__}: {ex}"[:200]}
+        else:
+            graph = {"unavailable": why or "capture failed on another rank"}
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
