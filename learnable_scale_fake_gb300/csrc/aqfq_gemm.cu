@@ -125,36 +125,48 @@ __device__ __forceinline__ bool aborted(GemmShared* sh) {
 }
 
 // expert and row group of grid row `slot` (groups of MT x 128 rows, experts
-// in order); one warp, result in *e / *mt (e = -1: no work)
+// in order); one warp, result in *e / *mt (e = -1: no work).  Experts are
+// taken 128 at a time, lane l holding experts l, l + 32, l + 64, l + 96: the
+// offsets of a batch are loaded together, one round trip per 128 experts.
 __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int slot, int* e_out,
                           int* mt_out) {
   const int lane = threadIdx.x & 31;
   int base = 0;
-  for (int64_t e0 = 0; e0 < E; e0 += 32) {
-    const int64_t e = e0 + lane;
-    int t = 0;
-    if (e < E) {
-      int64_t lo = off[e], hi = off[e + 1];
-      if (lo < 0) lo = 0;
-      if (hi > total_m) hi = total_m;
-      t = hi > lo ? int((hi - lo + MT * BM - 1) / (MT * BM)) : 0;  // groups of MT row tiles
-    }
-    int incl = t;
+  for (int64_t e0 = 0; e0 < E; e0 += 128) {
+    int64_t lo[4], hi[4];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-      if (lane >= d) incl += v;
+    for (int q = 0; q < 4; ++q) {
+      const int64_t e = e0 + q * 32 + lane;
+      lo[q] = e < E ? int64_t(off[e]) : 0;
+      hi[q] = e < E ? int64_t(off[e + 1]) : 0;
     }
-    const int excl = incl - t;
-    const bool hit = (e < E) && slot >= base + excl && slot < base + incl;
-    const unsigned mask = __ballot_sync(0xFFFFFFFFu, hit);
-    if (mask) {
-      const int src = __ffs(mask) - 1;
-      *e_out = (int)__shfl_sync(0xFFFFFFFFu, (int)e, src);
-      *mt_out = slot - base - __shfl_sync(0xFFFFFFFFu, excl, src);
-      return;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t e = e0 + q * 32 + lane;
+      int t = 0;
+      if (e < E) {
+        int64_t l = lo[q], h = hi[q];
+        if (l < 0) l = 0;
+        if (h > total_m) h = total_m;
+        t = h > l ? int((h - l + MT * BM - 1) / (MT * BM)) : 0;  // groups of MT row tiles
+      }
+      int incl = t;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      const int excl = incl - t;
+      const bool hit = (e < E) && slot >= base + excl && slot < base + incl;
+      const unsigned mask = __ballot_sync(0xFFFFFFFFu, hit);
+      if (mask) {
+        const int src = __ffs(mask) - 1;
+        *e_out = (int)__shfl_sync(0xFFFFFFFFu, (int)e, src);
+        *mt_out = slot - base - __shfl_sync(0xFFFFFFFFu, excl, src);
+        return;
+      }
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    base += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
   *e_out = -1;
   *mt_out = 0;
