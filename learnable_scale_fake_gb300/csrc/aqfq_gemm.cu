@@ -398,12 +398,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- weight producers (fake-quant into shared memory) ----
     const int pw = warp - 2 - (warp > kTmaWarp ? 1 : 0) - (warp > 9 ? 1 : 0);  // 0..7
     const int pt = pw * 32 + lane;                                              // 0..255
-    const float g = __ldg(a.tscale + e);
-    const bool gfast = (g >= 0x1p-64f) && (g <= 0x1p64f);
-    const float rg = gfast ? __frcp_rn(g) : __int_as_float(0x7FC00000), ng = -g;
-    if (pt < 128) stab[pt] = scale_entry(uint32_t(pt), g);
-    // the eight producer warps only: named barrier 1
-    asm volatile("bar.sync 1, %0;" ::"n"(kProducerThreads) : "memory");
     const int64_t kb = a.K / 16;
     const uint8_t* wrow = a.w + (size_t(e) * a.N + size_t(nt) * BN) * size_t(a.K) * 2;
     const float* srow = a.scale + (size_t(e) * a.N + size_t(nt) * BN) * size_t(kb);
@@ -416,12 +410,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     uint32_t xw[2][8];
     float sbv[2];
-    // prefetch step 0
+    // step 0's weights and block scales are in flight while the table is built
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       ld_stream(wrow + (size_t(n_[i]) * a.K + j_[i] * 16) * 2, xw[i]);
       sbv[i] = __ldg(srow + size_t(n_[i]) * kb + j_[i]);
     }
+    const float g = __ldg(a.tscale + e);
+    const bool gfast = (g >= 0x1p-64f) && (g <= 0x1p64f);
+    const float rg = gfast ? __frcp_rn(g) : __int_as_float(0x7FC00000), ng = -g;
+    if (pt < 128) stab[pt] = scale_entry(uint32_t(pt), g);
+    // the eight producer warps only: named barrier 1
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducerThreads) : "memory");
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % WS;
       uint32_t nx[2][8];
