@@ -116,6 +116,20 @@ def test_gemm_block_scale_quotient_at_e4m3_midpoints():
     assert np.array_equal(yb, rb), f"{np.count_nonzero(yb != rb)} of {yb.size} differ"
 
 
+def test_gemm_many_experts_beyond_one_search_batch():
+    """300 experts (the tile search takes experts 128 at a time), ragged sizes
+    with empty experts and one past a 512-row group: one-hot rows exact."""
+    rng = np.random.default_rng(41)
+    sizes = rng.integers(0, 40, 300)
+    sizes[::7] = 0
+    sizes[250] = 530
+    x, off, w, s, g = _inputs(300, 128, 64, sizes.tolist(), 250, onehot=True)
+    y = _run(x, off, w, s, g)
+    ref, _ = oracle.grouped_qdq_gemm(bits(x), off.numpy(), bits(w), s.numpy(), g.numpy())
+    yb, rb = bits(y), bits(torch.from_numpy(ref).to(torch.bfloat16))
+    assert np.array_equal(yb, rb), f"{np.count_nonzero(yb != rb)} of {yb.size} differ"
+
+
 def test_gemm_offsets_clamped_to_rows():
     """Offsets below 0 or beyond total_m are clamped to [0, total_m]: the kernel
     computes the clamped experts and touches no row outside Y."""
