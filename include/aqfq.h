@@ -165,7 +165,10 @@ aqfq_status aqfq_grouped_qdq(const aqfq_qspec* spec, const void* w, int64_t E, i
  *   workspace     device scratch, >= aqfq_scale_grad_workspace_bytes(...)
  *                 bytes (0 bytes for per-channel / per-group / NVFP4 learned;
  *                 per-tensor, per-head and the NVFP4 tensor scale need it; the
- *                 result is deterministic: fixed reduction order)
+ *                 result is deterministic: fixed reduction order).  Per-tensor
+ *                 and tensor-scale reductions keep a counter in its first 16
+ *                 bytes, which the call zeroes on the stream itself: the
+ *                 contents need no initialisation.
  * Per-head (x [T, H, D], scale [H], learnable per-head activation scale, e.g.
  * FP8 attention / KV activations; msModelSlim guide, "FA3Quant"): requires
  * H * D / 16 <= 2^24. */
@@ -185,7 +188,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
  * by every GPU that loads the library until the process exits) and allocates
  * nothing.  Arguments and results as aqfq_scale_grad without the workspace.
  *   - Returns AQFQ_ERR_WORKSPACE when aqfq_scale_grad_workspace_bytes(...)
- *     exceeds 128 KiB (16384 partial sums).
+ *     exceeds 128 KiB (a 16-byte counter and 16382 partial sums).
  *   - All calls share the array: calls whose kernels may overlap on the GPU
  *     (unordered streams) race.  Nothing needs clearing between calls.
  *   - The first call on a device looks the array's device address up (device

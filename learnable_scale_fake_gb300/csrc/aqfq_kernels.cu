@@ -16,7 +16,8 @@
 //   - per channel with long rows: one warp per row, per-lane double
 //     accumulation of chunk sums, double butterfly;
 //   - per tensor / NVFP4 tensor scale: per-CTA double partials into the
-//     caller's workspace, then a one-warp-per-entry pass in fixed order.
+//     caller's workspace; the last CTA to finish (a ticket zeroed on the
+//     stream before the launch) adds them, warp per entry, in fixed order.
 // Every order is fixed, so results are bit-reproducible run to run.
 #include "aqfq_internal.h"
 
@@ -140,7 +141,9 @@ struct GradArgs {
   const float* scale;
   const float* tscale;
   float* dscale;
-  double* ws;
+  double* ws;           // CTA partials [batch, nparts]
+  unsigned* ticket;     // RED = 1: CTAs done (zeroed by the launch before the kernel)
+  float* red_out;       // RED = 1: the per-batch-entry sums (dscale or the tensor-scale grads)
   int64_t batch, rows;
   uint32_t cpb;
   FastDiv cpr;
@@ -232,6 +235,27 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
       __syncthreads();
     }
   }
+  if constexpr (RED == 1) {
+    // the last CTA to finish adds every entry's partials in a fixed order:
+    // warp per entry, lane l takes partials l, l + 32, ..., then a butterfly
+    __shared__ int last;
+    if (threadIdx.x == 0) {
+      __threadfence();  // this CTA's partials before its ticket
+      last = atomicAdd(a.ticket, 1u) == gridDim.x * gridDim.y - 1u;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      const volatile double* ws = a.ws;
+      for (int64_t b = threadIdx.x >> 5; b < a.batch; b += kThreads / 32) {
+        double t = 0.0;
+        for (int i = lane; i < a.nparts; i += 32) t += ws[b * a.nparts + i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+        if (lane == 0) store_grad(a.red_out + b, (float)t, a.accumulate);
+      }
+    }
+  }
 }
 
 // per-channel gradient for rows whose K is not a power of two <= 512: one warp
@@ -272,20 +296,6 @@ __global__ void __launch_bounds__(kThreads, (RowTune<DX>::MINB)) scale_grad_row_
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
     if (lane == 0) store_grad(a.dscale + row, (float)acc, a.accumulate);
-  }
-}
-
-// sum of the CTA partials of each batch entry, in a fixed order
-__global__ void reduce_partials_kernel(const double* ws, int nparts, int64_t batch, float* out,
-                                       int accumulate) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); b < batch;
-       b += (int64_t)gridDim.x * (blockDim.x / 32)) {
-    double t = 0.0;
-    for (int i = lane; i < nparts; i += 32) t += ws[b * nparts + i];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-    if (lane == 0) store_grad(out + b, (float)t, accumulate);
   }
 }
 
@@ -536,7 +546,8 @@ size_t grad_workspace_bytes(const Problem& p) {
   if (p.fmt != F_NVFP4 && p.gran == G_HEAD)
     return size_t(head_threads(p, kMaxCtasPerSm)) * sizeof(double);
   if (!grad_needs_partials(p) || p.batch == 0) return 0;
-  return size_t(p.batch) * size_t(grad_parts(p, kMaxCtasPerSm)) * sizeof(double);
+  // a 16-byte header (the CTAs' ticket), then the partials
+  return 16 + size_t(p.batch) * size_t(grad_parts(p, kMaxCtasPerSm)) * sizeof(double);
 }
 
 namespace {
@@ -618,7 +629,9 @@ cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, c
   a.scale = scale;
   a.tscale = tscale;
   a.dscale = dscale;
-  a.ws = ws;
+  a.ws = partials ? ws + 2 : ws;  // after the 16-byte ticket header
+  a.ticket = partials ? reinterpret_cast<unsigned*>(ws) : nullptr;
+  a.red_out = out;
   a.batch = p.batch;
   a.rows = p.rows;
   a.cpb = p.cpb;
@@ -627,17 +640,15 @@ cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, c
   a.ir = IntRange{p.qmin, p.qmax};
   a.accumulate = accumulate;
   a.nparts = 0;
-  int nparts;
-  switch (p.fmt) {
-    case F_INT8: nparts = grad_fmt<F_INT8>(p, a, st); break;
-    case F_INT4: nparts = grad_fmt<F_INT4>(p, a, st); break;
-    case F_FP8: nparts = grad_fmt<F_FP8>(p, a, st); break;
-    default: nparts = grad_fmt<F_NVFP4>(p, a, st); break;
+  if (partials) {  // the ticket starts at zero on the stream, before the kernel
+    cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
   }
-  if (partials) {
-    int64_t blocks = (p.batch + 7) / 8;
-    if (blocks > 65535) blocks = 65535;
-    reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, nparts, p.batch, out, accumulate);
+  switch (p.fmt) {
+    case F_INT8: grad_fmt<F_INT8>(p, a, st); break;
+    case F_INT4: grad_fmt<F_INT4>(p, a, st); break;
+    case F_FP8: grad_fmt<F_FP8>(p, a, st); break;
+    default: grad_fmt<F_NVFP4>(p, a, st); break;
   }
   return cudaGetLastError();
 }

@@ -12,8 +12,9 @@
 // The array below is 128 KiB (16384 doubles).  It lives in every GPU that
 // loads the library until the process exits.  All calls share it: two calls
 // whose kernels overlap on the GPU (different streams, no ordering between
-// them) race on it.  Each call overwrites every partial it later reads, so
-// nothing has to be cleared between calls.
+// them) race on it.  Each call overwrites every partial it later reads and
+// zeroes the counter at its head on the stream, so nothing has to be cleared
+// between calls.
 //
 // The first call on a device looks the array's device address up with
 // cudaGetSymbolAddress while that device is current and caches it; make that

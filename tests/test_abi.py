@@ -119,7 +119,7 @@ def test_grad_argument_checks(L):
     assert big % (16 * 8) == 0 and 16 * 8 <= big < 100000 * 16 * 8
     assert aqfq.aqfq_scale_grad_workspace_bytes(I8, 1, 4, 64) == 0
     assert aqfq.aqfq_scale_grad_workspace_bytes(I4, 2, 8, 128) == 0
-    assert aqfq.aqfq_scale_grad_workspace_bytes(F8T, 3, 4, 64) == 3 * 8
+    assert aqfq.aqfq_scale_grad_workspace_bytes(F8T, 3, 4, 64) == 16 + 3 * 8  # counter + partials
     assert aqfq.aqfq_scale_grad_workspace_bytes(NV, 1, 4, 40) == 0  # rejected shape
 
 
