@@ -134,6 +134,23 @@ def test_scale_grad_accumulate_and_determinism(case):
     assert_grad_close(got, old.astype(np.float64) + r, ra, extra_abs=old, what="accumulated")
 
 
+@pytest.mark.parametrize("name", ["fp8_tensor", "nvfp4_dynamic"])
+def test_reduced_grad_batch_beyond_grid_limit(name):
+    """Per-tensor and NVFP4 tensor-scale gradients over 70000 batch entries
+    (above the 65535 grid-y limit: a CTA walks several entries, and the last
+    CTA to finish adds every entry's partials)."""
+    case = next(c for c in CASES if c[0] == name)
+    case = (case[0], case[1], (70000, 1, 32)) + case[3:]
+    sp = case[1]
+    x, dy, scale, ts = _inputs(case, seed=30)
+    ds, dts, _ = gpu_grad(sp, x, dy, scale, ts, want_dx=False)
+    ref = oracle_grad(sp, x, dy, scale, ts)
+    if dts is not None:
+        assert_grad_close(dts, ref["dtensor_scale"], ref["dtensor_scale_abs"], what="dtensor_scale")
+    else:
+        assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
+
+
 def test_per_head_grad_many_rounds():
     """x [T, H, D] large enough that each thread of the per-head gradient walks
     several tokens (more chunks than threads), with the STE input gradient."""
