@@ -87,23 +87,54 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def stored_traffic(op_name):
-    """DRAM bytes per launch of op `op_name` from the committed ncu summary
-    (profiles/traffic.md), if it was taken on the current state of the sources
-    its row names; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.md")
-    if not os.path.exists(p):
+    """DRAM bytes per launch of op `op_name` from the stored ncu capture
+    (profiles/traffic.json: op -> bytes, sources, their digest), if it was
+    taken on the current state of the sources it names; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            row = json.load(f)["ops"].get(op_name)
+    except (OSError, ValueError, KeyError, AttributeError):
         return None
-    for line in open(p):
-        tok = [t.strip() for t in line.strip().strip("|").split("|")]
-        if len(tok) >= 4 and tok[0] == op_name:
-            files = [f.strip() for f in tok[3].split(",") if f.strip()]
-            try:
-                if files and tok[2] == source_digest(files):
-                    return int(tok[1])
-            except (OSError, ValueError):
-                return None
+    if not row:
+        return None
+    try:
+        if row["sources"] and row["digest"] == source_digest(row["sources"]):
+            return int(row["dram_bytes_per_launch"])
+    except (OSError, KeyError, TypeError, ValueError):
+        return None
     return None
+
+
+def rank_plan(gpus, env):
+    """How this process serves `--gpus N`: "run" (a single process with N = 1,
+    or one rank of an N-rank launch), "spawn" (N > 1 outside a launcher: start
+    N ranks on this node), or an error message when the launcher's world size
+    disagrees with N."""
+    world = env.get("WORLD_SIZE")
+    if gpus < 1:
+        return "error: --gpus must be at least 1"
+    if world is None:
+        return "run" if gpus == 1 else "spawn"
+    if int(world) != gpus:
+        return f"error: --gpus {gpus} but the launcher started WORLD_SIZE={world} ranks"
+    return "run"
+
+
+def spawn_ranks(gpus, argv):
+    """Runs this script as `gpus` ranks of one node (torch.distributed.run,
+    rendezvous on 127.0.0.1) and returns the launcher's exit code."""
+    import socket
+
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 class Clocks:
@@ -376,6 +407,12 @@ def max_over_ranks(value, dist, device):
 
 def main():
     args = parse()
+    plan = rank_plan(args.gpus, os.environ)
+    if plan.startswith("error"):
+        print(f"bench.py: {plan}", file=sys.stderr)
+        sys.exit(2)
+    if plan == "spawn":
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     if args.impl == "reference":
         reference_arm(args)
         return

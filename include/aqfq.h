@@ -183,17 +183,22 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
  * over a scratch buffer: a plugin inside a framework that owns all device
  * memory through its own pool and gives the plugin no allocation hook, or a
  * latency-critical path where a cudaMalloc, which may synchronise the device,
- * is not acceptable.  This call takes the scratch of the per-tensor and
- * NVFP4 tensor-scale reductions from a 128 KiB array inside the library (held
- * by every GPU that loads the library until the process exits) and allocates
- * nothing.  Arguments and results as aqfq_scale_grad without the workspace.
+ * is not acceptable.  This call takes the scratch of the per-tensor, NVFP4
+ * tensor-scale and per-head reductions from a 128 KiB array inside the
+ * library (held by every GPU that loads the library until the process exits)
+ * and allocates nothing.  Arguments and results as aqfq_scale_grad without
+ * the workspace.
  *   - Returns AQFQ_ERR_WORKSPACE when aqfq_scale_grad_workspace_bytes(...)
- *     exceeds 128 KiB (a 16-byte counter and 16382 partial sums).
+ *     exceeds 128 KiB (a 16-byte counter and 16382 partial sums).  Per-tensor
+ *     and tensor-scale gradients fit for up to about 16380 batch entries;
+ *     per-head gradients (x [T, H, D]) fit only while T * H * D / 16 <= 16384.
  *   - All calls share the array: calls whose kernels may overlap on the GPU
  *     (unordered streams) race.  Nothing needs clearing between calls.
- *   - The first call on a device looks the array's device address up (device
- *     current at the call) and caches it; make that first call before any
- *     stream capture. */
+ *   - The array's device address is looked up for the device current at the
+ *     call, once per device and CUDA context (cached under the context's
+ *     unique ID, so a device reset leads to a fresh lookup).  The first call
+ *     on a device may load the library's device code there: make it before
+ *     any stream capture. */
 aqfq_status aqfq_scale_grad_noalloc(const aqfq_qspec* spec, const void* x, const void* dy,
                                     int64_t batch, int64_t rows, int64_t K, const float* scale,
                                     const float* tensor_scale, float* dscale,

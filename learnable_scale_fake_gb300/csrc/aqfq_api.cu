@@ -5,14 +5,17 @@
 
 namespace aqfq {
 
+// SM count of the current device, cached per device ordinal; 0 when the
+// device cannot be queried (the entry points that size grids or workspaces
+// from it then return AQFQ_ERR_CUDA instead of guessing)
 int sm_count() {
-  static int cache[256];  // per device ordinal; 0 = not yet queried
+  static int cache[256];  // 0 = not yet queried
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
   if (cache[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return 148;
+      return 0;
     cache[dev] = n;
   }
   return cache[dev];
@@ -162,6 +165,7 @@ size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, in
                                        int64_t K) {
   Problem p;
   if (make_problem(spec, batch, rows, K, p) != AQFQ_OK) return 0;
+  if (aqfq::sm_count() <= 0) return 0;
   return aqfq::grad_workspace_bytes(p);
 }
 
@@ -188,6 +192,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
   if (dx && !aligned(dx, 32)) return AQFQ_ERR_ALIGN;
   if ((dscale && !aligned(dscale, 4)) || (dtensor_scale && !aligned(dtensor_scale, 4)))
     return AQFQ_ERR_ALIGN;
+  if (aqfq::sm_count() <= 0) return AQFQ_ERR_CUDA;  // grids and workspace follow the SM count
   const size_t need = aqfq::grad_workspace_bytes(p);
   if (need > 0) {
     if (!workspace) return AQFQ_ERR_WORKSPACE;
@@ -207,6 +212,7 @@ aqfq_status aqfq_observer_minmax(const void* x, int64_t T, int64_t H, int64_t D,
   if ((!x && T * H * D > 0) || ((!min_out || !max_out) && H > 0)) return AQFQ_ERR_NULL;
   if (!aligned(x, 32)) return AQFQ_ERR_ALIGN;
   if (!aligned(min_out, 4) || !aligned(max_out, 4)) return AQFQ_ERR_ALIGN;
+  if (aqfq::sm_count() <= 0) return AQFQ_ERR_CUDA;
   return finish(aqfq::launch_observer(x, T, H, D, min_out, max_out, accumulate,
                                       static_cast<cudaStream_t>(stream)));
 }

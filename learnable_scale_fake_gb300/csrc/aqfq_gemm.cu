@@ -26,12 +26,9 @@
 // bytes) and W_hat (4 stages of 16 KiB; one arrival per producer warp), so the
 // producers can run up to three k-steps ahead of the MMAs; empty barriers are
 // armed by tcgen05.commit.
-// The CTAs of a cluster (kCN column tiles of the same row group) read the same
-// X tiles: each loads every kCN-th tile and multicasts it to all of them, and
-// every CTA's MMA commit releases an X stage in all of them (an X stage is
-// refilled only once every CTA has consumed it).  This divides the L2 reads
-// for X by kCN; the loads stay paced by each SM's intake of operand bytes,
-// which multicast does not change.
+// Every CTA loads its own X tiles (column tiles of one row group read the
+// same X rows from L2; the loads are paced by each SM's intake of operand
+// bytes, not by L2).
 // Every wait is bounded; on a timeout the CTA drains what it issued, frees
 // its tensor memory, raises the caller's error flag and returns.
 #include <cuda.h>
@@ -50,7 +47,6 @@ using namespace sm100;
 constexpr int BM = 128, BN = 128, BK = 64, MT = 4;
 constexpr int XS = 2;  // X ring stages (MT tiles of 16 KiB each)
 constexpr int WS = 4;  // fake-quantized weight ring stages (16 KiB each)
-constexpr int kCN = 2;  // CTAs per cluster: column tiles of one row group share X
 constexpr int kGemmThreads = 384;  // 12 warps
 constexpr int kMmaWarp = 1, kTmaWarp = 5;
 constexpr int kProducerThreads = 256;
@@ -80,42 +76,6 @@ struct __align__(8) GemmShared {
   int32_t abort;
   int32_t expert, mtile;
 };
-
-// ---- cluster forms of the TMA load and the MMA commit ------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 2D tile load written to the same shared-memory offset of every CTA in
-// `mask`, completion counted on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* tmap, uint64_t* bar,
-                                               int32_t c0, int32_t c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-// one arrival, once this thread's prior tcgen05 operations complete, on the
-// mbarrier at the same offset in every CTA of `mask`
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
 
 __device__ __forceinline__ void set_abort(GemmShared* sh) {
   atomicExch(&sh->abort, 1);
@@ -281,8 +241,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   GemmShared* sh = reinterpret_cast<GemmShared*>(smem + kRings);
   ScaleEntry* stab = reinterpret_cast<ScaleEntry*>(smem + kRings + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = int(cluster_ctarank()), ccount = int(cluster_nctarank());  // 1 or kCN
-  const uint16_t cmask = uint16_t((1u << ccount) - 1u);
 
   if (warp == 0) {
     int e, mt;
@@ -293,7 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       sh->abort = 0;
       for (int s = 0; s < XS; ++s) {
         mbar_init(&sh->full_x[s], 1);
-        mbar_init(&sh->empty_x[s], ccount);  // one commit from each CTA of the cluster
+        mbar_init(&sh->empty_x[s], 1);
       }
       for (int s = 0; s < WS; ++s) {
         mbar_init(&sh->full_w[s], kProducerThreads / 32);
@@ -306,10 +264,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
   const int e = sh->expert;
-  // grid rows beyond the last tile: no work, nothing allocated (a cluster's
-  // CTAs share the grid row, so they leave together)
+  // grid rows beyond the last tile: no work, nothing allocated
   if (e < 0) return;
-  cluster_sync();  // the peers' barriers are initialised before any multicast
   const int mt = sh->mtile;
   if (warp == kMmaWarp) tmem_alloc(&sh->tmem, kTmemCols);
   tc_fence_before_sync();
@@ -341,15 +297,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           set_abort(sh);
           break;
         }
-        mbar_arrive_expect_tx(&sh->full_x[s], kTileBytes * ntiles);  // every CTA's tiles
-        for (int i = crank; i < ntiles; i += ccount) {
-          if (ccount > 1)
-            tma_load_2d_mc(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full_x[s], kt * BK,
-                           int32_t(row0 + i * BM), cmask);
-          else
-            tma_load_2d(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full_x[s], kt * BK,
-                        int32_t(row0 + i * BM));
-        }
+        mbar_arrive_expect_tx(&sh->full_x[s], kTileBytes * ntiles);
+        for (int i = 0; i < ntiles; ++i)
+          tma_load_2d(tiles_a + s * kStageA + i * kTileBytes, &tmap_x, &sh->full_x[s], kt * BK,
+                      int32_t(row0 + i * BM));
         ++issued;
       }
       if (aborted(sh)) {
@@ -387,8 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc_mma_f16(tmem + uint32_t(i * BN), da + ((i * kTileBytes + kk * 32) >> 4),
                          db + ((kk * 32) >> 4), idesc, (kt | kk) != 0);
         }
-        if (ccount > 1) tc_commit_mc(&sh->empty_x[s], cmask);
-        else tc_commit(&sh->empty_x[s]);
+        tc_commit(&sh->empty_x[s]);
         tc_commit(&sh->empty_w[sw]);
       }
       tc_commit(&sh->accum);
@@ -520,8 +470,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // no CTA leaves while a peer's multicast loads or commits may still reach it
-  cluster_sync();
   if (threadIdx.x == 0 && aborted(sh) && a.err) atomicExch(a.err, 1);
 }
 
@@ -608,22 +556,10 @@ extern "C" aqfq_status aqfq_grouped_qdq_gemm(const void* x, const int32_t* m_off
   a.N = N;
   a.K = K;
   a.total_m = total_m;
-  // clusters of kCN column tiles when the column tiles divide evenly, else single CTAs
   const unsigned ntn = unsigned(N / BN);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = (ntn % kCN == 0) ? kCN : 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(ntn, unsigned(slots), 1);
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmem;
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_qdq_gemm_kernel, tm, a) == cudaSuccess ? AQFQ_OK
-                                                                                : AQFQ_ERR_CUDA;
+  grouped_qdq_gemm_kernel<<<dim3(ntn, unsigned(slots), 1), kGemmThreads, kGemmSmem,
+                            static_cast<cudaStream_t>(stream)>>>(tm, a);
+  return cudaGetLastError() == cudaSuccess ? AQFQ_OK : AQFQ_ERR_CUDA;
 }
 
 extern "C" aqfq_status aqfq_selftest_wait_timeout(int32_t* flag, uint32_t polls, void* stream) {

@@ -10,15 +10,29 @@
 // entry point takes it from a fixed array inside the library instead.
 //
 // The array below is 128 KiB (16384 doubles).  It lives in every GPU that
-// loads the library until the process exits.  All calls share it: two calls
-// whose kernels overlap on the GPU (different streams, no ordering between
-// them) race on it.  Each call overwrites every partial it later reads and
-// zeroes the counter at its head on the stream, so nothing has to be cleared
-// between calls.
+// loads the library until the process exits.  Three reductions take their
+// scratch from it:
+//   - per-tensor INT8 / INT4 / FP8 gradients and the NVFP4 tensor-scale
+//     gradient: a 16-byte counter and one double per CTA and batch entry
+//     (up to about 16380 batch entries);
+//   - per-head gradients (x [T, H, D]): one double per thread used, and the
+//     threads used are min(T * H * D / 16, one wave of the GPU), so a
+//     per-head call fits only while T * H * D / 16 <= 16384 (262144 elements).
+// Larger calls are rejected with AQFQ_ERR_WORKSPACE before anything runs.
+// All calls share the array: two calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on it.  Each call
+// overwrites every partial it later reads and zeroes the counter at its head
+// on the stream, so nothing has to be cleared between calls.
 //
-// The first call on a device looks the array's device address up with
-// cudaGetSymbolAddress while that device is current and caches it; make that
-// first call before any stream capture.  No call allocates memory.
+// Host code cannot use the array's name as a device address: the address is
+// looked up with cudaGetSymbolAddress while the device is current, once per
+// device and context, and cached under the context's unique ID; after a
+// device reset the new context has a new ID and the address is looked up
+// again.  The first call on a device (or after a reset) may load the
+// library's device code there, so make it before any stream capture.  No call
+// allocates memory.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "aqfq.h"
@@ -30,21 +44,51 @@ constexpr int kMaxDevices = 256;
 
 __device__ __align__(256) double g_scale_grad_scratch[kScratchBytes / sizeof(double)];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
 std::mutex g_mu;
 void* g_ptr[kMaxDevices];
+unsigned long long g_ctx[kMaxDevices];  // context ID the cached address belongs to
 
-// device address of the array on the current device (host code cannot use the
-// symbol's name as an address); NULL on failure
+void* driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return p;
+}
+
+// unique ID of the context current on this thread; 0 when there is none or it
+// cannot be read (the address is then looked up on every call)
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    get_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+    get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// device address of the array on the current device; NULL on failure
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scale_grad_scratch) != cudaSuccess) return nullptr;
-    g_ptr[dev] = p;
-  }
-  return g_ptr[dev];
+  const unsigned long long id = current_context_id();
+  if (id != 0 && g_ptr[dev] && g_ctx[dev] == id) return g_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scale_grad_scratch) != cudaSuccess || !p) return nullptr;
+  g_ptr[dev] = p;
+  g_ctx[dev] = current_context_id();  // the lookup made the device's context current
+  return p;
 }
 
 }  // namespace

@@ -1,17 +1,20 @@
-"""The C ABI without a GPU: the library loads, exports every entry point that
-include/aqfq.h declares, and rejects bad arguments on the host (the checks
-run before any CUDA call, so fake pointer values are safe here)."""
+"""The C ABI on the host: the library loads, exports every entry point that
+include/aqfq.h declares, and rejects bad arguments before any launch (the
+checks run before any kernel, so fake pointer values are safe here).  One
+test (marked gpu) checks the workspace sizes, which follow the current
+device's SM count."""
 import ctypes
 import os
 import re
 
 import pytest
+import torch
 
 from learnable_scale_fake_gb300 import _build, aqfq
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OK, NULL, SHAPE, ALIGN, UNSUP, WS = 0, 1, 2, 3, 4, 5
+OK, NULL, SHAPE, ALIGN, UNSUP, WS, CUDA = 0, 1, 2, 3, 4, 5, 6
 A = 0x10000  # a fake, 256-byte aligned "device" address
 
 
@@ -104,14 +107,33 @@ def test_grad_argument_checks(L):
     assert grad(L, NV, ds=None) == NULL
     assert grad(L, NV, dts=A) == UNSUP            # learned NVFP4 has a fixed tensor scale
     assert grad(L, NVD, scale=None) == NULL       # needs dtensor_scale
-    assert grad(L, NVD, scale=None, ds=None, dts=A) == WS
     assert grad(L, NVD, scale=None, ds=A, dts=A) == UNSUP
+    assert grad(L, NV, dy=A + 8) == ALIGN
+    assert grad(L, NV, dx=A + 8) == ALIGN
+    assert aqfq.aqfq_scale_grad_workspace_bytes(NV, 1, 4, 40) == 0  # rejected shape
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a device")
+def test_grad_without_a_device_is_a_cuda_error(L):
+    """Grids and workspaces follow the device's SM count: with no device to
+    query, the workspace bound is 0 and a call with valid arguments returns
+    AQFQ_ERR_CUDA instead of guessing a size (nothing is launched)."""
+    assert aqfq.aqfq_scale_grad_workspace_bytes(NVD, 1, 4, 64) == 0
+    assert aqfq.aqfq_scale_grad_workspace_bytes(F8T, 3, 4, 64) == 0
+    assert grad(L, NVD, scale=None, ds=None, dts=A) == CUDA
+    assert grad(L, NV) == CUDA
+
+
+@pytest.mark.gpu
+def test_grad_workspace_checks(L):
+    """Workspace sizes and their checks (they follow the current device's SM
+    count); every call here is rejected on the host before any launch."""
+    torch.zeros(1, device="cuda")  # a current device
+    assert grad(L, NVD, scale=None, ds=None, dts=A) == WS
     need = aqfq.aqfq_scale_grad_workspace_bytes(NVD, 1, 4, 64)
     assert need > 0 and need % 8 == 0
     assert grad(L, NVD, scale=None, ds=None, dts=A, ws=A, wsb=need - 8) == WS
     assert grad(L, NVD, scale=None, ds=None, dts=A, ws=A + 4, wsb=need) == ALIGN
-    assert grad(L, NV, dy=A + 8) == ALIGN
-    assert grad(L, NV, dx=A + 8) == ALIGN
     hd = aqfq.qspec(aqfq.FP8_E4M3, aqfq.PER_HEAD)
     assert grad(L, hd) == WS                      # per-head sums need a workspace
     assert aqfq.aqfq_scale_grad_workspace_bytes(hd, 1000, 4, 64) == 1000 * 16 * 8  # all tokens
@@ -120,7 +142,6 @@ def test_grad_argument_checks(L):
     assert aqfq.aqfq_scale_grad_workspace_bytes(I8, 1, 4, 64) == 0
     assert aqfq.aqfq_scale_grad_workspace_bytes(I4, 2, 8, 128) == 0
     assert aqfq.aqfq_scale_grad_workspace_bytes(F8T, 3, 4, 64) == 16 + 3 * 8  # counter + partials
-    assert aqfq.aqfq_scale_grad_workspace_bytes(NV, 1, 4, 40) == 0  # rejected shape
 
 
 def test_observer_argument_checks(L):

@@ -3,7 +3,9 @@ allocate device memory (for example a plugin whose host framework owns every
 byte of device memory, or a path where a synchronising cudaMalloc is not
 allowed).  Through the C ABI, its output must match aqfq_scale_grad with a
 caller-provided workspace, on two calls in a row (the built-in scratch is
-shared and reused), and sizes beyond its 128 KiB scratch are rejected."""
+shared and reused), and sizes beyond its 128 KiB scratch are rejected.  The
+cases cover every reduction that takes its scratch from the built-in array:
+per-tensor, NVFP4 tensor scale and per-head."""
 import ctypes
 
 import numpy as np
@@ -21,6 +23,8 @@ CASES = [
      (2, 96, 1024)),
     ("fp8_per_tensor", Q(aqfq.FP8_E4M3, aqfq.PER_TENSOR), (3, 80, 512)),
     ("nvfp4_learned", Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16), (2, 33, 208)),
+    # per-head partial sums: 64 * 4 * 128 / 16 = 2048 threads' doubles in the scratch
+    ("fp8_per_head", Q(aqfq.FP8_E4M3, aqfq.PER_HEAD), (64, 4, 128)),
 ]
 
 
