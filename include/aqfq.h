@@ -34,6 +34,11 @@
  *         (INT: v <= qmin or v >= qmax; FP: |v| >= largest finite value);
  *         d x_hat / d x = 1 if inactive, 0 if active.
  *
+ * Rows of K = 8 * odd elements (K % 8 == 0 but K % 16 != 0) are accepted for
+ * per-tensor, per-channel and per-head INT8 / INT4 / FP8 (8-element chunks);
+ * NVFP4 and per-group specs need K % 16 == 0 (their blocks and groups are 16
+ * elements or more).
+ *
  * Layouts (all row-major, K contiguous, BF16 as 16-bit patterns):
  *   x, y, dy, dx : [batch, rows, K]   (batch = experts E for stacks, else 1;
  *                                      [T, H, D] for per-head activations)
@@ -55,11 +60,16 @@
  * launched; a rejected call launches nothing and returns a status:
  *   AQFQ_ERR_NULL         a required pointer is NULL (a buffer with no
  *                         elements may be NULL)
- *   AQFQ_ERR_SHAPE        negative size, K % 16 != 0, K % group != 0, or a
- *                         size beyond the limits stated per call
- *   AQFQ_ERR_ALIGN        x / y / dy / dx not 32-byte aligned; codes not
- *                         8-byte (packed) or 16-byte (byte codes) aligned;
- *                         float arrays not 4-byte aligned; workspace not 8-byte
+ *   AQFQ_ERR_SHAPE        negative size, K % 8 != 0, K % 16 != 0 for NVFP4
+ *                         or any per-group spec (K % group != 0), or a size
+ *                         beyond the limits stated per call
+ *   AQFQ_ERR_ALIGN        x / y / dy / dx not 16-byte aligned (32-byte aligned
+ *                         tensors take 256-bit accesses, 16-byte aligned ones
+ *                         128-bit accesses; the results are the same); codes
+ *                         not aligned to one chunk's codes: 16 bytes (INT8 /
+ *                         FP8) or 8 bytes (INT4 / NVFP4) when K % 16 == 0,
+ *                         8 or 4 bytes when K = 8 * odd; float arrays not
+ *                         4-byte aligned; workspace not 8-byte
  *   AQFQ_ERR_UNSUPPORTED  a format / granularity / mode combination the
  *                         library does not implement
  *   AQFQ_ERR_WORKSPACE    workspace smaller than aqfq_scale_grad_workspace_bytes
@@ -134,7 +144,7 @@ typedef struct aqfq_qspec {
  *     by some deployment formats is 1 / tensor_scale).
  * (AngelSlim mcore_qad article, section 3: format names map 1:1 to the
  * deployment side's layouts; "QAT + DeepSpeed ZeRO-3": save_format=real.)
- * Limits: rows * K / 16 < 2^32 (per batch entry). */
+ * Limits: rows * K / 16 < 2^32 per batch entry (rows * K / 8 when K % 16 != 0). */
 aqfq_status aqfq_qdq_fwd(const aqfq_qspec* spec, const void* x, int64_t batch, int64_t rows,
                          int64_t K, const float* scale, const float* tensor_scale, void* y,
                          uint8_t* codes, uint8_t* block_codes, void* stream);
@@ -171,7 +181,7 @@ aqfq_status aqfq_grouped_qdq(const aqfq_qspec* spec, const void* w, int64_t E, i
  *                 contents need no initialisation.
  * Per-head (x [T, H, D], scale [H], learnable per-head activation scale, e.g.
  * FP8 attention / KV activations; msModelSlim guide, "FA3Quant"): requires
- * H * D / 16 <= 2^24. */
+ * H * D / 16 <= 2^24 (H * D / 8 when D % 16 != 0). */
 aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
                             int64_t rows, int64_t K, const float* scale,
                             const float* tensor_scale, float* dscale, float* dtensor_scale,
@@ -218,7 +228,8 @@ size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, in
  * result is +inf / -inf.
  * Source: msModelSlim guide, "FA3Quant" steps 3-4 (per-head local min/max,
  * min-of-mins / max-of-maxes merge).
- * Limits: D % 16 == 0; H * D / 16 <= 2^24. */
+ * Limits: D % 8 == 0; H * D / 16 <= 2^24 (H * D / 8 when D % 16 != 0); x
+ * 16-byte aligned. */
 aqfq_status aqfq_observer_minmax(const void* x, int64_t T, int64_t H, int64_t D, float* min_out,
                                  float* max_out, int accumulate, void* stream);
 

@@ -1,5 +1,7 @@
 // aqfq_api.cu -- the extern "C" entry points of libaqfq: argument checks on the
 // host, then the launches (include/aqfq.h documents every call).
+#include <initializer_list>
+
 #include "aqfq.h"
 #include "aqfq_internal.h"
 
@@ -33,15 +35,27 @@ bool pow2_in(int64_t v, int64_t lo, int64_t hi) {
   return v >= lo && v <= hi && (v & (v - 1)) == 0;
 }
 
-// Checks the spec and sizes; fills p.  Pointer checks are done by the callers.
+// Checks the spec and sizes; fills p (its chunk layout assumes 32-byte aligned
+// data until choose_layout sees the pointers).  Pointer checks are done by the
+// callers.
 aqfq_status make_problem(const aqfq_qspec* sp, int64_t batch, int64_t rows, int64_t K,
                          Problem& p) {
   if (!sp) return AQFQ_ERR_NULL;
-  if (batch < 0 || rows < 0 || K < 0 || K % 16 != 0) return AQFQ_ERR_SHAPE;
-  if (rows > 0 && K / 16 > int64_t(0xFFFFFFFF) / rows) return AQFQ_ERR_SHAPE;
-  const int64_t cpb = rows * (K / 16);
+  if (batch < 0 || rows < 0 || K < 0 || K % 8 != 0) return AQFQ_ERR_SHAPE;
+  const int ce = (K % 16 == 0) ? 16 : 8;
+  if (ce == 8) {
+    // rows of 8 * odd elements: only units that are whole rows, tensors or heads
+    const bool fmt_ok = sp->fmt == AQFQ_INT8 || sp->fmt == AQFQ_INT4 || sp->fmt == AQFQ_FP8_E4M3;
+    const bool gran_ok = sp->gran == AQFQ_PER_TENSOR || sp->gran == AQFQ_PER_CHANNEL ||
+                         sp->gran == AQFQ_PER_HEAD;
+    if (!fmt_ok || !gran_ok) return AQFQ_ERR_SHAPE;
+  }
+  if (rows > 0 && K / ce > int64_t(0xFFFFFFFF) / rows) return AQFQ_ERR_SHAPE;
+  const int64_t cpb = rows * (K / ce);
   if (cpb > int64_t(0xFFFFFFFF)) return AQFQ_ERR_SHAPE;
   if (batch > 0 && cpb > 0 && batch > (int64_t(1) << 62) / (cpb * 32)) return AQFQ_ERR_SHAPE;
+  p.ce = ce;
+  p.lay = ce == 16 ? aqfq::L_32 : aqfq::L_8;
   p.fmt = sp->fmt;
   p.gran = sp->gran;
   p.group = sp->group;
@@ -50,7 +64,7 @@ aqfq_status make_problem(const aqfq_qspec* sp, int64_t batch, int64_t rows, int6
   p.rows = rows;
   p.K = K;
   p.cpb = uint32_t(cpb);
-  p.cpr = uint32_t(K / 16);
+  p.cpr = uint32_t(K / ce);
   p.qmin = float(sp->qmin);
   p.qmax = float(sp->qmax);
   switch (sp->fmt) {
@@ -93,7 +107,30 @@ aqfq_status make_problem(const aqfq_qspec* sp, int64_t batch, int64_t rows, int6
 
 bool byte_codes(const Problem& p) { return p.fmt == AQFQ_INT8 || p.fmt == AQFQ_FP8_E4M3; }
 
-int64_t elems(const Problem& p) { return p.batch * int64_t(p.cpb) * 16; }
+int64_t elems(const Problem& p) { return p.batch * int64_t(p.cpb) * p.ce; }
+
+// The chunk layout for these BF16 tensors (NULL ones ignored): 16-element
+// chunks with 256-bit accesses when every tensor is 32-byte aligned, with
+// 128-bit accesses when one is only 16-byte aligned; 8-element chunks (K % 16
+// != 0) need 16 bytes.  AQFQ_ERR_ALIGN below 16 bytes.
+aqfq_status choose_layout(Problem& p, std::initializer_list<const void*> tensors) {
+  bool a32 = true;
+  for (const void* t : tensors) {
+    if (!t) continue;
+    if (!aligned(t, 16)) return AQFQ_ERR_ALIGN;
+    a32 = a32 && aligned(t, 32);
+  }
+  if (p.ce == 16) p.lay = a32 ? aqfq::L_32 : aqfq::L_16;
+  else p.lay = aqfq::L_8;
+  return AQFQ_OK;
+}
+
+// codes: one byte per element (INT8 / FP8) or one nibble (INT4 / NVFP4); a
+// chunk's codes are stored in one access
+bool codes_aligned(const Problem& p, const void* codes) {
+  const int bytes = byte_codes(p) ? p.ce : p.ce / 2;
+  return aligned(codes, uintptr_t(bytes));
+}
 
 // number of learned scales (0 in NVFP4 dynamic mode)
 int64_t scale_count(const Problem& p) {
@@ -146,8 +183,8 @@ aqfq_status aqfq_qdq_fwd(const aqfq_qspec* spec, const void* x, int64_t batch, i
   const bool any = elems(p) > 0;
   if (any && (!x || (!y && !codes))) return AQFQ_ERR_NULL;
   if ((s = check_scales(p, scale, tensor_scale)) != AQFQ_OK) return s;
-  if (!aligned(x, 32) || !aligned(y, 32)) return AQFQ_ERR_ALIGN;
-  if (codes && !aligned(codes, byte_codes(p) ? 16 : 8)) return AQFQ_ERR_ALIGN;
+  if ((s = choose_layout(p, {x, y})) != AQFQ_OK) return s;
+  if (codes && !codes_aligned(p, codes)) return AQFQ_ERR_ALIGN;
   if (block_codes && p.fmt != AQFQ_NVFP4) return AQFQ_ERR_UNSUPPORTED;
   if (codes && p.fmt == AQFQ_NVFP4 && !block_codes) return AQFQ_ERR_NULL;
   if (block_codes && !codes) return AQFQ_ERR_NULL;
@@ -177,7 +214,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
   Problem p;
   aqfq_status s = make_problem(spec, batch, rows, K, p);
   if (s != AQFQ_OK) return s;
-  if (p.gran == AQFQ_PER_HEAD && p.rows * (p.K / 16) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
+  if (p.gran == AQFQ_PER_HEAD && p.rows * int64_t(p.cpr) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
   if (elems(p) > 0 && (!x || !dy)) return AQFQ_ERR_NULL;
   if ((s = check_scales(p, scale, tensor_scale)) != AQFQ_OK) return s;
   const bool dyn = p.fmt == AQFQ_NVFP4 && p.mode == AQFQ_SCALE_DYNAMIC_BLOCK;
@@ -188,8 +225,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
     if (!dscale && scale_count(p) > 0) return AQFQ_ERR_NULL;
     if (dtensor_scale) return AQFQ_ERR_UNSUPPORTED;
   }
-  if (!aligned(x, 32) || !aligned(dy, 32)) return AQFQ_ERR_ALIGN;
-  if (dx && !aligned(dx, 32)) return AQFQ_ERR_ALIGN;
+  if ((s = choose_layout(p, {x, dy, dx})) != AQFQ_OK) return s;
   if ((dscale && !aligned(dscale, 4)) || (dtensor_scale && !aligned(dtensor_scale, 4)))
     return AQFQ_ERR_ALIGN;
   if (aqfq::sm_count() <= 0) return AQFQ_ERR_CUDA;  // grids and workspace follow the SM count
@@ -206,14 +242,16 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
 
 aqfq_status aqfq_observer_minmax(const void* x, int64_t T, int64_t H, int64_t D, float* min_out,
                                  float* max_out, int accumulate, void* stream) {
-  if (T < 0 || H < 0 || D < 0 || D % 16 != 0) return AQFQ_ERR_SHAPE;
-  if (H * (D / 16) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
-  if (T > 0 && H * (D / 16) > 0 && T > (int64_t(1) << 40) / (H * (D / 16))) return AQFQ_ERR_SHAPE;
+  if (T < 0 || H < 0 || D < 0 || D % 8 != 0) return AQFQ_ERR_SHAPE;
+  const int64_t ce = (D % 16 == 0) ? 16 : 8;
+  if (H * (D / ce) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
+  if (T > 0 && H * (D / ce) > 0 && T > (int64_t(1) << 40) / (H * (D / ce))) return AQFQ_ERR_SHAPE;
   if ((!x && T * H * D > 0) || ((!min_out || !max_out) && H > 0)) return AQFQ_ERR_NULL;
-  if (!aligned(x, 32)) return AQFQ_ERR_ALIGN;
+  if (!aligned(x, 16)) return AQFQ_ERR_ALIGN;
   if (!aligned(min_out, 4) || !aligned(max_out, 4)) return AQFQ_ERR_ALIGN;
   if (aqfq::sm_count() <= 0) return AQFQ_ERR_CUDA;
-  return finish(aqfq::launch_observer(x, T, H, D, min_out, max_out, accumulate,
+  const int lay = ce == 8 ? aqfq::L_8 : (aligned(x, 32) ? aqfq::L_32 : aqfq::L_16);
+  return finish(aqfq::launch_observer(x, T, H, D, lay, min_out, max_out, accumulate,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -233,7 +271,7 @@ aqfq_status aqfq_scale_init(const aqfq_qspec* spec, const void* x, int64_t batch
   if (s != AQFQ_OK) return s;
   if (!x && elems(p) > 0) return AQFQ_ERR_NULL;
   if ((s = check_scales(p, scale, tensor_scale)) != AQFQ_OK) return s;
-  if (!aligned(x, 32)) return AQFQ_ERR_ALIGN;
+  if ((s = choose_layout(p, {x})) != AQFQ_OK) return s;
   return finish(aqfq::launch_scale_init(p, x, scale, tensor_scale,
                                         static_cast<cudaStream_t>(stream)));
 }

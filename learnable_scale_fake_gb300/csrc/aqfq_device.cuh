@@ -4,7 +4,11 @@
 // load per operand, one NVFP4 block, 1/8 of an INT4 g128 group.  Every kernel
 // maps one lane to one chunk at a time, so loads are perfectly coalesced
 // (a warp streams 1 KiB contiguous per operand) and an NVFP4 block's amax and
-// gradient sum never leave the lane.
+// gradient sum never leave the lane.  Three chunk layouts (Lay):
+//   L_32  16 elements, one 256-bit access per operand (32-byte aligned data)
+//   L_16  16 elements, two 128-bit accesses (data only 16-byte aligned)
+//   L_8   8 elements, one 128-bit access (rows of K = 8 * odd elements; only
+//         per-tensor, per-channel and per-head INT8 / INT4 / FP8 use it)
 //
 // Rounding steps follow the library's contract (include/aqfq.h):
 //   v = x / s        the IEEE binary32 quotient: per chunk one correctly rounded
@@ -26,7 +30,15 @@
 namespace aqfq {
 
 constexpr int kThreads = 256;  // threads per CTA for every streaming kernel
-constexpr int kChunk = 16;     // elements per lane-chunk
+constexpr int kChunk = 16;     // elements per lane-chunk (L_32, L_16)
+
+enum Lay { L_32 = 0, L_16 = 1, L_8 = 2 };
+// 32-bit words (two BF16 each) of a chunk, and its bytes
+template <int L>
+struct LayT {
+  static constexpr int NW = L == L_8 ? 4 : 8;
+  static constexpr int BYTES = NW * 4;
+};
 
 enum Fmt { F_INT8 = 0, F_INT4 = 1, F_FP8 = 2, F_NVFP4 = 3 };
 enum Gran { G_TENSOR = 0, G_ROW = 1, G_GROUP = 2, G_HEAD = 3 };
@@ -65,6 +77,18 @@ __device__ __forceinline__ void ld_stream(const void* p, uint32_t (&w)[8]) {
       : "l"(p));
 }
 
+__device__ __forceinline__ void ld_stream_v4(const void* p, uint32_t& a, uint32_t& b, uint32_t& c,
+                                             uint32_t& d) {
+  // (the evict-first L2 priority exists only for 256-bit accesses)
+  asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+      : "l"(p));
+}
+
+__device__ __forceinline__ void st_32(void* p, uint32_t a) {
+  asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ void st_256(void* p, const uint32_t (&w)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
                "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -78,6 +102,44 @@ __device__ __forceinline__ void st_128(void* p, uint32_t a, uint32_t b, uint32_t
 
 __device__ __forceinline__ void st_64(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// chunk gc of a BF16 tensor in layout L
+template <int L>
+__device__ __forceinline__ void ld_chunk(const uint8_t* base, uint64_t gc,
+                                         uint32_t (&w)[LayT<L>::NW]) {
+  const uint8_t* p = base + gc * LayT<L>::BYTES;
+  if constexpr (L == L_32) {
+    ld_stream(p, w);
+  } else {
+    ld_stream_v4(p, w[0], w[1], w[2], w[3]);
+    if constexpr (L == L_16) ld_stream_v4(p + 16, w[4], w[5], w[6], w[7]);
+  }
+}
+
+template <int L>
+__device__ __forceinline__ void st_chunk(uint8_t* base, uint64_t gc,
+                                         const uint32_t (&w)[LayT<L>::NW]) {
+  uint8_t* p = base + gc * LayT<L>::BYTES;
+  if constexpr (L == L_32) {
+    st_256(p, w);
+  } else {
+    st_128(p, w[0], w[1], w[2], w[3]);
+    if constexpr (L == L_16) st_128(p + 16, w[4], w[5], w[6], w[7]);
+  }
+}
+
+// packed codes of chunk gc: INT8 / FP8 one byte per element, INT4 / NVFP4 one
+// nibble (cw holds them in order, element 0 lowest)
+template <int L, bool BYTE_CODES>
+__device__ __forceinline__ void st_codes(uint8_t* codes, uint64_t gc, const uint32_t (&cw)[4]) {
+  if constexpr (L == L_8) {
+    if constexpr (BYTE_CODES) st_64(codes + gc * 8, cw[0], cw[1]);
+    else st_32(codes + gc * 4, cw[0]);
+  } else {
+    if constexpr (BYTE_CODES) st_128(codes + gc * 16, cw[0], cw[1], cw[2], cw[3]);
+    else st_64(codes + gc * 8, cw[0], cw[1]);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -210,10 +272,11 @@ __device__ __forceinline__ float nvfp4_block_scale(float sb, float g, uint32_t& 
 }
 
 // largest |x| of a chunk as binary32 (exact: a BF16 value)
-__device__ __forceinline__ float chunk_amax(const uint32_t (&w)[8]) {
+template <int NW>
+__device__ __forceinline__ float chunk_amax(const uint32_t (&w)[NW]) {
   uint32_t m = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  for (int i = 0; i < NW; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
   uint32_t a = max(m & 0xFFFFu, m >> 16);
   return __uint_as_float(a << 16);
 }
@@ -349,13 +412,13 @@ __device__ __forceinline__ uint32_t code_signs(uint32_t sgn) {
   else return ((sgn >> 12) & 0x8u) | ((sgn >> 24) & 0x80u);
 }
 
-template <int FMT, bool CODES>
-__device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[8], const Divisor& d,
-                                               const IntRange& r, uint32_t (&yw)[8],
+template <int FMT, bool CODES, int NW>
+__device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[NW], const Divisor& d,
+                                               const IntRange& r, uint32_t (&yw)[NW],
                                                uint32_t (&cw)[4]) {
   if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NW; ++i) {
     uint32_t code = 0;
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
       // the integer grid maps +-0 alike (an integer code has no sign)
@@ -377,13 +440,13 @@ __device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[8], const Di
   }
 }
 
-template <int FMT, bool DX>
-__device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const uint32_t (&dw)[8],
+template <int FMT, bool DX, int NW>
+__device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
                                                  const Divisor& d, const IntRange& r,
-                                                 uint32_t (&dxw)[8]) {
-  float t[16];
+                                                 uint32_t (&dxw)[NW]) {
+  float t[2 * NW];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NW; ++i) {
     // the sign of a zero quotient does not change a gradient term
     const float v0 = mdiv(bf_lo(xw[i]), d), v1 = mdiv(bf_hi(xw[i]), d);
     bool k0, k1;
@@ -406,9 +469,9 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const 
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
 #pragma unroll
-  for (int w = 1; w < 16; w *= 2) {
+  for (int w = 1; w < 2 * NW; w *= 2) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+    for (int i = 0; i < 2 * NW; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
   }
   return t[0];
 }
@@ -417,13 +480,13 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[8], const 
 // One chunk, forward, IEEE division per element (any scale; only chunks
 // outside the fast path's bounds come here): y = bf16(q * s)
 // ---------------------------------------------------------------------------
-template <int FMT, bool CODES>
-__device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[8], float s, const IntRange& r,
-                                          uint32_t (&yw)[8], uint32_t (&cw)[4]) {
+template <int FMT, bool CODES, int NW>
+__device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[NW], float s, const IntRange& r,
+                                          uint32_t (&yw)[NW], uint32_t (&cw)[4]) {
   if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
   const bool zero = (s == 0.0f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NW; ++i) {
     const float x0 = bf_lo(xw[i]), x1 = bf_hi(xw[i]);
     const float v0 = zero ? sign_zero(x0) : __fdiv_rn(x0, s);
     const float v1 = zero ? sign_zero(x1) : __fdiv_rn(x1, s);
@@ -443,13 +506,13 @@ __device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[8], float s, cons
 // in binary32 (q and v are within a factor of two, Sterbenz), so the only
 // roundings are one per product and four levels of the tree.
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX>
-__device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[8], const uint32_t (&dw)[8],
-                                            float s, const IntRange& r, uint32_t (&dxw)[8]) {
-  float t[16];
+template <int FMT, bool DX, int NW>
+__device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
+                                            float s, const IntRange& r, uint32_t (&dxw)[NW]) {
+  float t[2 * NW];
   const bool zero = (s == 0.0f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NW; ++i) {
     const float x0 = bf_lo(xw[i]), x1 = bf_hi(xw[i]);
     const float v0 = zero ? sign_zero(x0) : __fdiv_rn(x0, s);
     const float v1 = zero ? sign_zero(x1) : __fdiv_rn(x1, s);
@@ -464,9 +527,9 @@ __device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[8], const uint3
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
 #pragma unroll
-  for (int w = 1; w < 16; w *= 2) {
+  for (int w = 1; w < 2 * NW; w *= 2) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
+    for (int i = 0; i < 2 * NW; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
   }
   return t[0];
 }

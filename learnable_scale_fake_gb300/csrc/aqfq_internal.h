@@ -12,13 +12,17 @@
 
 namespace aqfq {
 
-// A validated problem: x is [batch, rows, K] BF16, K % 16 == 0.
+// A validated problem: x is [batch, rows, K] BF16, K % 8 == 0.  Chunks are
+// 16 elements when K % 16 == 0, else 8 (per-tensor, per-channel and per-head
+// INT8 / INT4 / FP8 only); lay is the chunk layout the launch uses (Lay).
 struct Problem {
   int fmt, gran, group, mode;
   float qmin, qmax;
   int64_t batch, rows, K;
-  uint32_t cpb;  // 16-element chunks per batch entry = rows * K / 16
-  uint32_t cpr;  // chunks per row = K / 16
+  int ce;        // elements per chunk: 16 or 8
+  int lay;       // L_32, L_16 or L_8
+  uint32_t cpb;  // chunks per batch entry = rows * K / ce
+  uint32_t cpr;  // chunks per row = K / ce
 };
 
 int sm_count();
@@ -35,8 +39,8 @@ cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, c
                               int accumulate, double* ws, cudaStream_t st);
 
 // statistics (stats.cu)
-cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, float* mn, float* mx,
-                            int accumulate, cudaStream_t st);
+cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, int lay, float* mn,
+                            float* mx, int accumulate, cudaStream_t st);
 cudaError_t launch_minmax_scale(const float* mn, const float* mx, int64_t H, float qmax,
                                 float* scale, cudaStream_t st);
 cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, float* tscale,

@@ -75,8 +75,9 @@ struct FwdArgs {
   IntRange ir;
 };
 
-template <int FMT, int GRAN, bool DYN, bool CODES, int U>
+template <int FMT, int GRAN, bool DYN, bool CODES, int U, int L>
 __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
+  constexpr int NW = LayT<L>::NW;
   for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
     const uint64_t base = (uint64_t)b * a.cpb;
     float g = 0.0f, st = 0.0f;
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
     if constexpr (GRAN == G_TENSOR) st = __ldg(a.scale + b);
     for (uint64_t c0 = (uint64_t)blockIdx.x * (kThreads * U); c0 < a.cpb;
          c0 += (uint64_t)gridDim.x * (kThreads * U)) {
-      uint32_t xw[U][8];
+      uint32_t xw[U][NW];
       float sraw[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
         sraw[j] = st;
         if (c < a.cpb) {
           const uint64_t gc = base + c;
-          ld_stream(a.x + gc * 32, xw[j]);
+          ld_chunk<L>(a.x, gc, xw[j]);
           if constexpr (FMT == F_NVFP4) {
             if constexpr (!DYN) sraw[j] = __ldg(a.scale + gc);
           } else if constexpr (GRAN == G_ROW) {
@@ -116,17 +117,13 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
           const float sb = DYN ? __fdiv_rn(amax, 6.0f) : sraw[j];
           s = nvfp4_block_scale(sb, g, ecode);
         }
-        uint32_t yw[8], cw[4];
+        uint32_t yw[NW], cw[4];
         const Divisor dv = make_divisor(s, amax);
         if (dv.fast) qdq_chunk_fast<FMT, CODES>(xw[j], dv, a.ir, yw, cw);
         else qdq_chunk<FMT, CODES>(xw[j], s, a.ir, yw, cw);
-        if (a.y) st_256(a.y + gc * 32, yw);  // NULL: export of the codes only
+        if (a.y) st_chunk<L>(a.y, gc, yw);  // NULL: export of the codes only
         if constexpr (CODES) {
-          if constexpr (FMT == F_INT8 || FMT == F_FP8) {
-            st_128(a.codes + gc * 16, cw[0], cw[1], cw[2], cw[3]);
-          } else {
-            st_64(a.codes + gc * 8, cw[0], cw[1]);
-          }
+          st_codes<L, FMT == F_INT8 || FMT == F_FP8>(a.codes, gc, cw);
           if constexpr (FMT == F_NVFP4) a.bcodes[gc] = (uint8_t)ecode;
         }
       }
@@ -159,9 +156,10 @@ __device__ __forceinline__ void store_grad(float* p, float g, int accumulate) {
 
 // RED = 0: one scale per aligned run of (1 << lg) lanes, written directly.
 // RED = 1: one scale (or NVFP4 tensor scale) per batch entry, CTA partials.
-template <int FMT, int GRAN, bool DYN, bool DX, int RED, int U>
+template <int FMT, int GRAN, bool DYN, bool DX, int RED, int U, int L>
 __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
     scale_grad_kernel(const GradArgs a) {
+  constexpr int NW = LayT<L>::NW;
   const int lane = threadIdx.x & 31;
   for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
     const uint64_t base = (uint64_t)b * a.cpb;
@@ -171,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
     double acc = 0.0;
     for (uint64_t c0 = (uint64_t)blockIdx.x * (kThreads * U); c0 < a.cpb;
          c0 += (uint64_t)gridDim.x * (kThreads * U)) {
-      uint32_t xw[U][8], dw[U][8];
+      uint32_t xw[U][NW], dw[U][NW];
       float sraw[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
@@ -179,8 +177,8 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
         sraw[j] = st;
         if (c < a.cpb) {
           const uint64_t gc = base + c;
-          ld_stream(a.x + gc * 32, xw[j]);
-          ld_stream(a.dy + gc * 32, dw[j]);
+          ld_chunk<L>(a.x, gc, xw[j]);
+          ld_chunk<L>(a.dy, gc, dw[j]);
           if constexpr (GRAN == G_GROUP && !DYN) sraw[j] = __ldg(a.scale + (gc >> a.lg));
         }
       }
@@ -199,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
             s = nvfp4_block_scale(sb, g, ecode);
             dec = dec_e4m3x2(ecode).x;
           }
-          uint32_t dxw[8];
+          uint32_t dxw[NW];
           const Divisor dv = make_divisor(s);
           bool slow = !dv.fast;
           if (dv.fast) {
@@ -207,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
             slow = isnan(cs);  // a quotient overflowed: redo the chunk exactly
           }
           if (slow) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
-          if constexpr (DX) st_256(a.dx + gc * 32, dxw);
+          if constexpr (DX) st_chunk<L>(a.dx, gc, dxw);
         }
         if constexpr (RED == 0) {
           const int width = 1 << a.lg;
@@ -260,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
 
 // per-channel gradient for rows whose K is not a power of two <= 512: one warp
 // per row, lanes stride over the row's chunks
-template <int FMT, bool DX, int U>
+template <int FMT, bool DX, int U, int L>
 __global__ void __launch_bounds__(kThreads, (RowTune<DX>::MINB)) scale_grad_row_kernel(const GradArgs a) {
+  constexpr int NW = LayT<L>::NW;
   const int lane = threadIdx.x & 31;
   const int64_t nrows = a.batch * a.rows;
   const uint32_t cpr = a.cpr.d;
@@ -272,24 +271,24 @@ __global__ void __launch_bounds__(kThreads, (RowTune<DX>::MINB)) scale_grad_row_
     const uint64_t base = (uint64_t)row * cpr;
     double acc = 0.0;
     for (uint32_t c0 = 0; c0 < cpr; c0 += 32 * U) {
-      uint32_t xw[U][8], dw[U][8];
+      uint32_t xw[U][NW], dw[U][NW];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         const uint32_t c = c0 + j * 32 + lane;
         if (c < cpr) {
-          ld_stream(a.x + (base + c) * 32, xw[j]);
-          ld_stream(a.dy + (base + c) * 32, dw[j]);
+          ld_chunk<L>(a.x, base + c, xw[j]);
+          ld_chunk<L>(a.dy, base + c, dw[j]);
         }
       }
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         const uint32_t c = c0 + j * 32 + lane;
         if (c < cpr) {
-          uint32_t dxw[8];
+          uint32_t dxw[NW];
           float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw) : 0.0f;
           if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
           acc += (double)cs;
-          if constexpr (DX) st_256(a.dx + (base + c) * 32, dxw);
+          if constexpr (DX) st_chunk<L>(a.dx, base + c, dxw);
         }
       }
     }
@@ -319,32 +318,33 @@ struct HeadArgs {
   IntRange ir;
 };
 
-template <int FMT, bool DX>
+template <int FMT, bool DX, int L>
 __global__ void __launch_bounds__(kThreads) scale_grad_head_kernel(const HeadArgs a) {
+  constexpr int NW = LayT<L>::NW;
   const uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   if (j >= a.used) return;
   const float s = __ldg(a.scale + fdiv((uint32_t)(j % a.cpt), a.cph));
   const Divisor dv = make_divisor(s);
   double acc = 0.0;
   for (uint64_t c0 = j; c0 < a.nchunks; c0 += 2 * a.used) {
-    uint32_t xw[2][8], dw[2][8];
+    uint32_t xw[2][NW], dw[2][NW];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const uint64_t c = c0 + u * a.used;
       if (c < a.nchunks) {
-        ld_stream(a.x + c * 32, xw[u]);
-        ld_stream(a.dy + c * 32, dw[u]);
+        ld_chunk<L>(a.x, c, xw[u]);
+        ld_chunk<L>(a.dy, c, dw[u]);
       }
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const uint64_t c = c0 + u * a.used;
       if (c >= a.nchunks) continue;
-      uint32_t dxw[8];
+      uint32_t dxw[NW];
       float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[u], dw[u], dv, a.ir, dxw) : 0.0f;
       if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[u], dw[u], s, a.ir, dxw);
       acc += (double)cs;
-      if constexpr (DX) st_256(a.dx + c * 32, dxw);
+      if constexpr (DX) st_chunk<L>(a.dx, c, dxw);
     }
   }
   a.ws[j] = acc;
@@ -399,35 +399,57 @@ dim3 stream_grid(uint32_t cpb, int64_t batch, int U, int cap) {
   return dim3((unsigned)gx, (unsigned)gy, 1);
 }
 
-template <int FMT, int GRAN, bool DYN, bool CODES>
+template <int FMT, int GRAN, bool DYN, bool CODES, int L>
 void fwd_launch(const FwdArgs& a, cudaStream_t st) {
   constexpr int U = kFwdU;
   if (U > 1 && a.cpb >= uint32_t(U) * kThreads) {
-    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, U><<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
+    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, U, L>
+        <<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
   } else {
-    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 1><<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
+    qdq_fwd_kernel<FMT, GRAN, DYN, CODES, 1, L>
+        <<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
   }
 }
 
-template <int FMT, bool CODES>
+// L_8 (rows of 8 * odd elements) exists only for the granularities whose unit
+// is a whole row, a whole tensor or a head; the host checks never send a
+// block or group format there
+template <int FMT, bool CODES, int L>
 void fwd_gran(const Problem& p, const FwdArgs& a, cudaStream_t st) {
   if constexpr (FMT == F_NVFP4) {
-    if (p.mode == 1) fwd_launch<FMT, G_GROUP, true, CODES>(a, st);
-    else fwd_launch<FMT, G_GROUP, false, CODES>(a, st);
+    static_assert(L != L_8, "NVFP4 blocks are 16 elements");
+    if (p.mode == 1) fwd_launch<FMT, G_GROUP, true, CODES, L>(a, st);
+    else fwd_launch<FMT, G_GROUP, false, CODES, L>(a, st);
   } else {
     switch (p.gran) {
-      case G_TENSOR: fwd_launch<FMT, G_TENSOR, false, CODES>(a, st); break;
-      case G_ROW: fwd_launch<FMT, G_ROW, false, CODES>(a, st); break;
-      case G_GROUP: fwd_launch<FMT, G_GROUP, false, CODES>(a, st); break;
-      default: fwd_launch<FMT, G_HEAD, false, CODES>(a, st); break;
+      case G_TENSOR: fwd_launch<FMT, G_TENSOR, false, CODES, L>(a, st); break;
+      case G_ROW: fwd_launch<FMT, G_ROW, false, CODES, L>(a, st); break;
+      case G_GROUP:
+        if constexpr (L != L_8) fwd_launch<FMT, G_GROUP, false, CODES, L>(a, st);
+        break;
+      default: fwd_launch<FMT, G_HEAD, false, CODES, L>(a, st); break;
     }
   }
 }
 
-template <int FMT>
+template <int FMT, int L>
 void fwd_codes(const Problem& p, const FwdArgs& a, cudaStream_t st) {
-  if (a.codes) fwd_gran<FMT, true>(p, a, st);
-  else fwd_gran<FMT, false>(p, a, st);
+  if (a.codes) fwd_gran<FMT, true, L>(p, a, st);
+  else fwd_gran<FMT, false, L>(p, a, st);
+}
+
+template <int FMT>
+void fwd_lay(const Problem& p, const FwdArgs& a, cudaStream_t st) {
+  if constexpr (FMT == F_NVFP4) {
+    if (p.lay == L_32) fwd_codes<FMT, L_32>(p, a, st);
+    else fwd_codes<FMT, L_16>(p, a, st);
+  } else {
+    switch (p.lay) {
+      case L_32: fwd_codes<FMT, L_32>(p, a, st); break;
+      case L_16: fwd_codes<FMT, L_16>(p, a, st); break;
+      default: fwd_codes<FMT, L_8>(p, a, st); break;
+    }
+  }
 }
 
 // unroll actually used by a gradient launch (U of the traits, or 1 when the
@@ -457,58 +479,73 @@ int grad_unit_lg(const Problem& p) {
   if (p.fmt == F_NVFP4) return 0;
   if (p.gran == G_GROUP) return log2_exact(p.group / 16);
   if (p.gran == G_ROW) {
-    const int l = log2_exact(p.K / 16);
+    const int l = log2_exact(p.cpr);
     return (l >= 0 && l <= 5) ? l : -1;
   }
   return 0;
 }
 
 // returns the CTAs per batch entry of a partial-sum launch (0 otherwise)
-template <int FMT, int GRAN, bool DYN, bool DX, int RED>
+template <int FMT, int GRAN, bool DYN, bool DX, int RED, int L>
 int grad_launch(const Problem& p, GradArgs a, cudaStream_t st) {
   constexpr int U = GradTune<FMT, DYN, DX, RED>::U;
   if constexpr (RED == 1) {
-    auto k = scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>;
+    auto k = scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1, L>;
     a.nparts = grad_parts(p, occupancy(k));
     k<<<stream_grid(a.cpb, a.batch, 1, a.nparts), kThreads, 0, st>>>(a);
     return a.nparts;
   } else {
     if (U > 1 && grad_unroll(a.cpb, U) == U) {
-      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U>
+      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U, L>
           <<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
     } else {
-      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1>
+      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1, L>
           <<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
     }
     return 0;
   }
 }
 
-template <int FMT, bool DX>
+template <int FMT, bool DX, int L>
 int grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
   if constexpr (FMT == F_NVFP4) {
-    if (p.mode == 1) return grad_launch<FMT, G_GROUP, true, DX, 1>(p, a, st);
-    return grad_launch<FMT, G_GROUP, false, DX, 0>(p, a, st);
+    static_assert(L != L_8, "NVFP4 blocks are 16 elements");
+    if (p.mode == 1) return grad_launch<FMT, G_GROUP, true, DX, 1, L>(p, a, st);
+    return grad_launch<FMT, G_GROUP, false, DX, 0, L>(p, a, st);
   } else {
     if (p.gran == G_TENSOR) {
-      return grad_launch<FMT, G_TENSOR, false, DX, 1>(p, a, st);
-    } else if (a.lg >= 0) {  // per-group, or per-channel rows of 16..512 (power of two)
-      return grad_launch<FMT, G_GROUP, false, DX, 0>(p, a, st);
+      return grad_launch<FMT, G_TENSOR, false, DX, 1, L>(p, a, st);
+    } else if (a.lg >= 0) {  // per-group, or per-channel rows of 1..32 chunks (power of two)
+      return grad_launch<FMT, G_GROUP, false, DX, 0, L>(p, a, st);
     } else {
       const int64_t nrows = p.batch * p.rows;
       int64_t blocks = (nrows + kThreads / 32 - 1) / (kThreads / 32);
       if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
       if (blocks < 1) blocks = 1;
-      scale_grad_row_kernel<FMT, DX, RowTune<DX>::U><<<(unsigned)blocks, kThreads, 0, st>>>(a);
+      scale_grad_row_kernel<FMT, DX, RowTune<DX>::U, L><<<(unsigned)blocks, kThreads, 0, st>>>(a);
       return 0;
     }
   }
 }
 
+template <int FMT, int L>
+int grad_dx(const Problem& p, const GradArgs& a, cudaStream_t st) {
+  if (a.dx) return grad_dispatch<FMT, true, L>(p, a, st);
+  return grad_dispatch<FMT, false, L>(p, a, st);
+}
+
 template <int FMT>
 int grad_fmt(const Problem& p, const GradArgs& a, cudaStream_t st) {
-  if (a.dx) return grad_dispatch<FMT, true>(p, a, st);
-  return grad_dispatch<FMT, false>(p, a, st);
+  if constexpr (FMT == F_NVFP4) {
+    if (p.lay == L_32) return grad_dx<FMT, L_32>(p, a, st);
+    return grad_dx<FMT, L_16>(p, a, st);
+  } else {
+    switch (p.lay) {
+      case L_32: return grad_dx<FMT, L_32>(p, a, st);
+      case L_16: return grad_dx<FMT, L_16>(p, a, st);
+      default: return grad_dx<FMT, L_8>(p, a, st);
+    }
+  }
 }
 
 }  // namespace
@@ -532,10 +569,10 @@ cudaError_t launch_qdq_fwd(const Problem& p, const void* x, const float* scale,
   if (p.fmt == F_NVFP4) a.lg = 0;
   a.ir = IntRange{p.qmin, p.qmax};
   switch (p.fmt) {
-    case F_INT8: fwd_codes<F_INT8>(p, a, st); break;
-    case F_INT4: fwd_codes<F_INT4>(p, a, st); break;
-    case F_FP8: fwd_codes<F_FP8>(p, a, st); break;
-    default: fwd_codes<F_NVFP4>(p, a, st); break;
+    case F_INT8: fwd_lay<F_INT8>(p, a, st); break;
+    case F_INT4: fwd_lay<F_INT4>(p, a, st); break;
+    case F_FP8: fwd_lay<F_FP8>(p, a, st); break;
+    default: fwd_lay<F_NVFP4>(p, a, st); break;
   }
   return cudaGetLastError();
 }
@@ -553,19 +590,28 @@ size_t grad_workspace_bytes(const Problem& p) {
 namespace {
 
 // returns the threads used (one wave of the kernel's resident CTAs)
-template <int FMT, bool DX>
+template <int FMT, bool DX, int L>
 uint64_t head_launch(const Problem& p, HeadArgs a, cudaStream_t st) {
-  auto k = scale_grad_head_kernel<FMT, DX>;
+  auto k = scale_grad_head_kernel<FMT, DX, L>;
   a.used = head_threads(p, occupancy(k));
   const uint64_t blocks = (a.used + kThreads - 1) / kThreads;
   k<<<(unsigned)blocks, kThreads, 0, st>>>(a);
   return a.used;
 }
 
+template <int FMT, int L>
+uint64_t head_dx(const Problem& p, const HeadArgs& a, cudaStream_t st) {
+  if (a.dx) return head_launch<FMT, true, L>(p, a, st);
+  return head_launch<FMT, false, L>(p, a, st);
+}
+
 template <int FMT>
 uint64_t head_fmt(const Problem& p, const HeadArgs& a, cudaStream_t st) {
-  if (a.dx) return head_launch<FMT, true>(p, a, st);
-  return head_launch<FMT, false>(p, a, st);
+  switch (p.lay) {
+    case L_32: return head_dx<FMT, L_32>(p, a, st);
+    case L_16: return head_dx<FMT, L_16>(p, a, st);
+    default: return head_dx<FMT, L_8>(p, a, st);
+  }
 }
 
 cudaError_t launch_head_grad(const Problem& p, const void* x, const void* dy, const float* scale,

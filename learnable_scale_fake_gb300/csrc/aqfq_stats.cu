@@ -59,9 +59,11 @@ __global__ void observer_keys_out(float* mn, float* mx, int64_t H) {
 
 constexpr int kObsU = 4;
 
+template <int L>
 __global__ void __launch_bounds__(kThreads)
     observer_reduce(const uint8_t* x, uint64_t nchunks, uint32_t cpt, FastDiv cph, uint64_t used,
                     uint32_t* kmn, uint32_t* kmx) {
+  constexpr int NW = LayT<L>::NW;
   const uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
   const bool active = j < used;
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -69,17 +71,17 @@ __global__ void __launch_bounds__(kThreads)
   if (active) {
     head = fdiv((uint32_t)(j % cpt), cph);
     for (uint64_t c0 = j; c0 < nchunks; c0 += used * kObsU) {
-      uint32_t w[kObsU][8];
+      uint32_t w[kObsU][NW];
 #pragma unroll
       for (int u = 0; u < kObsU; ++u) {
         const uint64_t c = c0 + u * used;
-        if (c < nchunks) ld_stream(x + c * 32, w[u]);
+        if (c < nchunks) ld_chunk<L>(x, c, w[u]);
       }
 #pragma unroll
       for (int u = 0; u < kObsU; ++u) {
         if (c0 + u * used < nchunks) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < NW; ++i) {
             const uint32_t k = key16x2(w[u][i]);
             lo = __vminu2(lo, k);
             hi = __vmaxu2(hi, k);
@@ -137,8 +139,9 @@ struct InitArgs {
 // Units of 1 << lg aligned lanes (NVFP4 blocks, groups): butterfly max, the
 // first lane of the unit stores amax / qmax.  The NVFP4 tensor amax still goes
 // through one atomicMax per warp.
-template <bool NVFP4>
+template <bool NVFP4, int L>
 __global__ void __launch_bounds__(kThreads) amax_direct_kernel(const InitArgs a) {
+  constexpr int NW = LayT<L>::NW;
   const int lane = threadIdx.x & 31;
   const int width = 1 << a.lg;
   float* scale = reinterpret_cast<float*>(a.sbits);
@@ -150,8 +153,8 @@ __global__ void __launch_bounds__(kThreads) amax_direct_kernel(const InitArgs a)
       const uint64_t c = c0 + threadIdx.x;
       uint32_t am = 0;
       if (c < a.cpb) {
-        uint32_t w[8];
-        ld_stream(a.x + (base + c) * 32, w);
+        uint32_t w[NW];
+        ld_chunk<L>(a.x, base + c, w);
         am = __float_as_uint(chunk_amax(w));
       }
       tmax = max(tmax, am);
@@ -169,8 +172,9 @@ __global__ void __launch_bounds__(kThreads) amax_direct_kernel(const InitArgs a)
   }
 }
 
-template <int GRAN, bool NVFP4>
+template <int GRAN, int L>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const InitArgs a) {
+  constexpr int NW = LayT<L>::NW;
   const int lane = threadIdx.x & 31;
   for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
     const uint64_t base = (uint64_t)b * a.cpb;
@@ -181,11 +185,10 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const InitArgs a) {
       uint32_t am = 0;
       int64_t unit = -1;
       if (c < a.cpb) {
-        uint32_t w[8];
-        ld_stream(a.x + (base + c) * 32, w);
+        uint32_t w[NW];
+        ld_chunk<L>(a.x, base + c, w);
         am = __float_as_uint(chunk_amax(w));
-        if constexpr (NVFP4) unit = (int64_t)(base + c);
-        else if constexpr (GRAN == G_TENSOR) unit = b;
+        if constexpr (GRAN == G_TENSOR) unit = b;
         else if constexpr (GRAN == G_ROW) unit = b * a.rows + fdiv((uint32_t)c, a.cpr);
         else if constexpr (GRAN == G_HEAD) unit = fdiv((uint32_t)c, a.cpr);
         else unit = (int64_t)((base + c) >> a.lg);
@@ -203,11 +206,6 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const InitArgs a) {
         if (unit >= 0 && (lane == 0 || prev != unit)) atomicMax(a.sbits + unit, am);
       }
     }
-    if constexpr (NVFP4) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) tmax = max(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, off));
-      if (lane == 0) atomicMax(a.tbits + b, tmax);
-    }
   }
 }
 
@@ -224,29 +222,60 @@ unsigned small_grid(int64_t n) {
   return (unsigned)b;
 }
 
+// scale-init kernels of 16-element-chunk layouts
+template <int L>
+void init_launch(const Problem& p, const InitArgs& a, dim3 grid, bool nvfp4, bool direct,
+                 cudaStream_t st) {
+  if (nvfp4) {
+    amax_direct_kernel<true, L><<<grid, kThreads, 0, st>>>(a);
+  } else if (direct) {
+    amax_direct_kernel<false, L><<<grid, kThreads, 0, st>>>(a);
+  } else {
+    switch (p.gran) {
+      case G_TENSOR: amax_kernel<G_TENSOR, L><<<grid, kThreads, 0, st>>>(a); break;
+      case G_ROW: amax_kernel<G_ROW, L><<<grid, kThreads, 0, st>>>(a); break;
+      case G_HEAD: amax_kernel<G_HEAD, L><<<grid, kThreads, 0, st>>>(a); break;
+      default: amax_kernel<G_GROUP, L><<<grid, kThreads, 0, st>>>(a); break;
+    }
+  }
+}
+
+template <int L>
+void observer_launch(const uint8_t* x, uint64_t nchunks, uint32_t cpt, FastDiv cph, uint32_t* kmn,
+                     uint32_t* kmx, cudaStream_t st) {
+  // threads used: one wave of the kernel's resident CTAs, as a multiple of
+  // the chunks per token
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, observer_reduce<L>, kThreads, 0) !=
+          cudaSuccess || occ < 1)
+    occ = 1;
+  uint64_t want = uint64_t(sm_count()) * occ * kThreads;
+  if (want > nchunks) want = nchunks;
+  uint64_t used = want / cpt * cpt;
+  if (used < cpt) used = cpt;
+  const uint64_t blocks = (used + kThreads - 1) / kThreads;
+  observer_reduce<L><<<(unsigned)blocks, kThreads, 0, st>>>(x, nchunks, cpt, cph, used, kmn, kmx);
+}
+
 }  // namespace
 
-cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, float* mn, float* mx,
-                            int accumulate, cudaStream_t st) {
+cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, int lay, float* mn,
+                            float* mx, int accumulate, cudaStream_t st) {
   if (H == 0) return cudaSuccess;
   observer_keys_in<<<small_grid(H), 256, 0, st>>>(mn, mx, H, accumulate);
-  const uint64_t cpt = uint64_t(H) * uint64_t(D / 16);
+  const uint32_t ce = lay == L_8 ? 8 : 16;
+  const uint64_t cpt = uint64_t(H) * uint64_t(D / ce);
   const uint64_t nchunks = uint64_t(T) * cpt;
   if (nchunks > 0) {
-    // threads used: one wave of the kernel's resident CTAs, as a multiple of
-    // the chunks per token
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, observer_reduce, kThreads, 0) !=
-            cudaSuccess || occ < 1)
-      occ = 1;
-    uint64_t want = uint64_t(sm_count()) * occ * kThreads;
-    if (want > nchunks) want = nchunks;
-    uint64_t used = want / cpt * cpt;
-    if (used < cpt) used = cpt;
-    const uint64_t blocks = (used + kThreads - 1) / kThreads;
-    observer_reduce<<<(unsigned)blocks, kThreads, 0, st>>>(
-        static_cast<const uint8_t*>(x), nchunks, (uint32_t)cpt, make_fastdiv((uint32_t)(D / 16)),
-        used, reinterpret_cast<uint32_t*>(mn), reinterpret_cast<uint32_t*>(mx));
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const FastDiv cph = make_fastdiv((uint32_t)(D / ce));
+    uint32_t* kmn = reinterpret_cast<uint32_t*>(mn);
+    uint32_t* kmx = reinterpret_cast<uint32_t*>(mx);
+    switch (lay) {
+      case L_32: observer_launch<L_32>(xb, nchunks, (uint32_t)cpt, cph, kmn, kmx, st); break;
+      case L_16: observer_launch<L_16>(xb, nchunks, (uint32_t)cpt, cph, kmn, kmx, st); break;
+      default: observer_launch<L_8>(xb, nchunks, (uint32_t)cpt, cph, kmn, kmx, st); break;
+    }
   }
   observer_keys_out<<<small_grid(H), 256, 0, st>>>(mn, mx, H);
   return cudaGetLastError();
@@ -293,17 +322,16 @@ cudaError_t launch_scale_init(const Problem& p, const void* x, float* scale, flo
     uint64_t gx = (uint64_t(p.cpb) + kThreads - 1) / kThreads;
     if (gx > 0x7FFFFFFFull) gx = 0x7FFFFFFFull;
     dim3 grid((unsigned)gx, (unsigned)(p.batch < 65535 ? p.batch : 65535), 1);
-    if (nvfp4) {
-      amax_direct_kernel<true><<<grid, kThreads, 0, st>>>(a);
-    } else if (direct) {
-      amax_direct_kernel<false><<<grid, kThreads, 0, st>>>(a);
-    } else {
-      switch (p.gran) {
-        case G_TENSOR: amax_kernel<G_TENSOR, false><<<grid, kThreads, 0, st>>>(a); break;
-        case G_ROW: amax_kernel<G_ROW, false><<<grid, kThreads, 0, st>>>(a); break;
-        case G_HEAD: amax_kernel<G_HEAD, false><<<grid, kThreads, 0, st>>>(a); break;
-        default: amax_kernel<G_GROUP, false><<<grid, kThreads, 0, st>>>(a); break;
+    if (p.lay == L_8) {
+      switch (p.gran) {  // rows of 8 * odd elements: tensors, rows and heads only
+        case G_TENSOR: amax_kernel<G_TENSOR, L_8><<<grid, kThreads, 0, st>>>(a); break;
+        case G_ROW: amax_kernel<G_ROW, L_8><<<grid, kThreads, 0, st>>>(a); break;
+        default: amax_kernel<G_HEAD, L_8><<<grid, kThreads, 0, st>>>(a); break;
       }
+    } else if (p.lay == L_32) {
+      init_launch<L_32>(p, a, grid, nvfp4, direct, st);
+    } else {
+      init_launch<L_16>(p, a, grid, nvfp4, direct, st);
     }
   }
   const float qmax = nvfp4 ? 6.0f : (p.fmt == F_FP8 ? 448.0f : p.qmax);

@@ -193,11 +193,14 @@ static float nvfp4_block_scale(float sb, float g, int* ecode) {
 /* Validation                                                                 */
 /* ------------------------------------------------------------------------- */
 
+/* Rows are whole multiples of 8 elements (the library's boundary); the NVFP4
+   block and every group (16 elements or more) need K to be a multiple of
+   their size. */
 static int spec_ok(const orc_spec* sp, int64_t K) {
   if (!sp) return 0;
-  if (K % 16 != 0) return 0;
+  if (K % 8 != 0) return 0;
   if (sp->fmt == ORC_NVFP4) {
-    return sp->gran == ORC_PER_GROUP && sp->group == 16 &&
+    return K % 16 == 0 && sp->gran == ORC_PER_GROUP && sp->group == 16 &&
            (sp->mode == ORC_SCALE_LEARNED || sp->mode == ORC_SCALE_DYNAMIC_BLOCK);
   }
   if (sp->mode != ORC_SCALE_LEARNED) return 0;

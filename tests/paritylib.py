@@ -58,17 +58,32 @@ def canaries_intact(whole, n, align_elems):
     return bool((head == 0xA5).all()) and bool((tail == 0xA5).all())
 
 
-def gpu_fwd(sp, x, scale, ts, codes=True, grouped=False):
+def on_device(t, misalign=False):
+    """t on the GPU, contiguous; misalign: at an address that is 16-byte but
+    not 32-byte aligned (inside a slightly larger buffer)."""
+    d = dev()
+    if not misalign:
+        return t.to(d).contiguous()
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=d)
+    v = buf[8:].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+def gpu_fwd(sp, x, scale, ts, codes=True, grouped=False, misalign=False):
     """Runs the forward on the GPU with guard-banded outputs; returns numpy
-    (y bits, codes, block codes)."""
+    (y bits, codes, block codes).  misalign: x and y 16-byte but not 32-byte
+    aligned."""
     d = dev()
     x3 = as3(x)
     B, R, K = x3.shape
-    xd = x3.to(d).contiguous()
+    xd = on_device(x3, misalign)
     sd = None if scale is None else scale.to(d)
     td = None if ts is None else ts.to(d)
     n = B * R * K
-    y, yw = guarded(n, torch.bfloat16, d, 64)
+    ya = 72 if misalign else 64  # guard band in elements (144 bytes: 16 mod 32)
+    y, yw = guarded(n, torch.bfloat16, d, ya)
     y = y.view(B, R, K)
     c = cw = b = bw = None
     nc = aqfq.codes_numel(sp, B, R, K)
@@ -81,7 +96,7 @@ def gpu_fwd(sp, x, scale, ts, codes=True, grouped=False):
     else:
         aqfq.aqfq_qdq_fwd(sp, xd, sd, td, y, c, b)
     torch.cuda.synchronize()
-    assert canaries_intact(yw, n, 64), "write outside y"
+    assert canaries_intact(yw, n, ya), "write outside y"
     if codes:
         assert canaries_intact(cw, nc, 256), "write outside codes"
         if b is not None:
@@ -91,12 +106,13 @@ def gpu_fwd(sp, x, scale, ts, codes=True, grouped=False):
     return bits(y), out_c, out_b
 
 
-def gpu_grad(sp, x, dy, scale, ts, want_dx=True, accumulate_from=None):
-    """Runs the scale gradient on the GPU; returns numpy (dscale, dtensor_scale, dx bits)."""
+def gpu_grad(sp, x, dy, scale, ts, want_dx=True, accumulate_from=None, misalign=False):
+    """Runs the scale gradient on the GPU; returns numpy (dscale, dtensor_scale,
+    dx bits).  misalign: x, dy and dx 16-byte but not 32-byte aligned."""
     d = dev()
     x3, dy3 = as3(x), as3(dy)
     B, R, K = x3.shape
-    xd, dyd = x3.to(d).contiguous(), dy3.to(d).contiguous()
+    xd, dyd = on_device(x3, misalign), on_device(dy3, misalign)
     sd = None if scale is None else scale.to(d)
     td = None if ts is None else ts.to(d)
     dyn = sp.fmt == aqfq.NVFP4 and sp.mode == aqfq.SCALE_DYNAMIC_BLOCK
@@ -111,8 +127,9 @@ def gpu_grad(sp, x, dy, scale, ts, want_dx=True, accumulate_from=None):
         if accumulate_from is not None:
             ds.copy_(torch.as_tensor(accumulate_from, dtype=torch.float32))
     dx = dxw = None
+    xa = 72 if misalign else 64
     if want_dx:
-        dx, dxw = guarded(B * R * K, torch.bfloat16, d, 64)
+        dx, dxw = guarded(B * R * K, torch.bfloat16, d, xa)
         dx = dx.view(B, R, K)
     wsb = aqfq.aqfq_scale_grad_workspace_bytes(sp, B, R, K)
     ws = torch.empty(max(wsb // 8, 1), dtype=torch.float64, device=d) if wsb else None
@@ -124,7 +141,7 @@ def gpu_grad(sp, x, dy, scale, ts, want_dx=True, accumulate_from=None):
     else:
         assert canaries_intact(dsw, n_s, 16)
     if want_dx:
-        assert canaries_intact(dxw, B * R * K, 64)
+        assert canaries_intact(dxw, B * R * K, xa)
     return (None if ds is None else ds.cpu().numpy(), None if dts is None else dts.cpu().numpy(),
             None if dx is None else bits(dx))
 

@@ -75,7 +75,8 @@ def test_forward_argument_checks(L):
     assert fwd(L, NV, scale=None) == NULL
     assert fwd(L, NV, K=24) == SHAPE
     assert fwd(L, NV, R=-1) == SHAPE
-    assert fwd(L, NV, x=A + 16) == ALIGN
+    assert fwd(L, NV, x=A + 8) == ALIGN           # BF16 tensors: 16-byte aligned at least
+    assert fwd(L, I8, y=A + 24) == ALIGN
     assert fwd(L, NV, y=A + 2) == ALIGN
     assert fwd(L, NV, scale=A + 2) == ALIGN
     assert fwd(L, NV, codes=A + 4, blk=A) == ALIGN
@@ -83,6 +84,11 @@ def test_forward_argument_checks(L):
     assert fwd(L, I8, codes=A + 8) == ALIGN      # byte codes are 16-byte aligned
     assert fwd(L, I8, blk=A, codes=A) == UNSUP   # block codes are NVFP4 only
     assert fwd(L, I4, K=192) == SHAPE            # K % group
+    assert fwd(L, I8, K=20) == SHAPE             # K % 8
+    assert fwd(L, I4, K=136) == SHAPE            # K = 8 * odd: no group or block formats
+    assert fwd(L, I8, K=24, codes=A + 4) == ALIGN  # 8-element chunks: byte codes 8-byte aligned
+    I4C = aqfq.qspec(aqfq.INT4, aqfq.PER_CHANNEL, qmin=-8, qmax=7)
+    assert fwd(L, I4C, K=24, codes=A + 2) == ALIGN  # and nibble codes 4-byte aligned
     assert fwd(L, aqfq.qspec(aqfq.NVFP4, aqfq.PER_GROUP, group=32)) == UNSUP
     assert fwd(L, aqfq.qspec(aqfq.NVFP4, aqfq.PER_CHANNEL, group=16)) == UNSUP
     assert fwd(L, aqfq.qspec(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-129, qmax=127)) == UNSUP
@@ -111,6 +117,27 @@ def test_grad_argument_checks(L):
     assert grad(L, NV, dy=A + 8) == ALIGN
     assert grad(L, NV, dx=A + 8) == ALIGN
     assert aqfq.aqfq_scale_grad_workspace_bytes(NV, 1, 4, 40) == 0  # rejected shape
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers pass the checks: no device only")
+def test_boundary_accepts_rows_of_eight_and_sixteen_byte_alignment(L):
+    """K % 8 == 0 rows (per-tensor / per-channel / per-head INT8, INT4, FP8) and
+    BF16 tensors that are 16-byte but not 32-byte aligned pass every host
+    check; without a device the call then fails at the launch (AQFQ_ERR_CUDA)."""
+    I4C = aqfq.qspec(aqfq.INT4, aqfq.PER_CHANNEL, qmin=-8, qmax=7)
+    F8H = aqfq.qspec(aqfq.FP8_E4M3, aqfq.PER_HEAD)
+    CUDA_ = 6
+    assert fwd(L, I8, K=24) == CUDA_
+    assert fwd(L, I8, K=8, codes=A + 8) == CUDA_
+    assert fwd(L, I4C, K=56, codes=A + 4) == CUDA_
+    assert fwd(L, F8T, K=40) == CUDA_
+    assert fwd(L, F8H, K=24) == CUDA_
+    assert fwd(L, NV, x=A + 16, y=A + 48) == CUDA_
+    assert fwd(L, I4, K=128, x=A + 16) == CUDA_
+    assert grad(L, I8, K=24, dx=A + 16) == CUDA_
+    assert grad(L, NV, x=A + 16, dy=A + 48) == CUDA_
+    assert L.aqfq_observer_minmax(A + 16, 4, 2, 24, A, 2 * A, 0, None) == CUDA_
+    assert L.aqfq_scale_init(ctypes.byref(I8), A + 16, 1, 4, 24, A, None, None) == CUDA_
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a device")
@@ -146,10 +173,11 @@ def test_grad_workspace_checks(L):
 
 def test_observer_argument_checks(L):
     f = L.aqfq_observer_minmax
-    assert f(A, 4, 2, 24, A, 2 * A, 0, None) == SHAPE
+    assert f(A, 4, 2, 12, A, 2 * A, 0, None) == SHAPE
     assert f(A, -1, 2, 16, A, 2 * A, 0, None) == SHAPE
     assert f(None, 4, 2, 16, A, 2 * A, 0, None) == NULL
-    assert f(A + 16, 4, 2, 16, A, 2 * A, 0, None) == ALIGN
+    assert f(A + 8, 4, 2, 16, A, 2 * A, 0, None) == ALIGN
+    assert f(A, 4, 2, 20, A, 2 * A, 0, None) == SHAPE   # D % 8
     assert f(A, 4, 1 << 21, 256, A, 2 * A, 0, None) == SHAPE
     m = L.aqfq_minmax_scale
     assert m(A, A, 4, ctypes.c_float(0.0), A, None) == SHAPE

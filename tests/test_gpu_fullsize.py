@@ -28,7 +28,9 @@ def _free():
 
 
 def _run(wl):
+    # the workload's set-up (inputs, scale init) ran on the current stream
     st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(st):
         wl.step(st)
     torch.cuda.synchronize()

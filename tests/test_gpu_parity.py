@@ -57,6 +57,18 @@ CASES = [
      (1e-4, 4e-4), None),
     ("nvfp4_learned", NV, (3, 45, 208), _x_t, (2e-3, 2e-2), (2e-5, 1e-4)),
     ("nvfp4_dynamic", NVD, (3, 41, 192), _x_act, None, (1e-4, 1e-2)),
+    # rows of K = 8 * odd elements (8-element chunks, 128-bit accesses)
+    ("int8_channel_k24", Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127), (2, 37, 24),
+     _x_normal, (1e-4, 4e-4), None),
+    ("int8_channel_k8", Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127), (2, 41, 8),
+     _x_normal, (1e-4, 4e-4), None),
+    ("fp8_channel_k520", Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL), (1, 23, 520), _x_normal,
+     (2e-5, 2e-4), None),
+    ("int4_channel_k56", Q(aqfq.INT4, aqfq.PER_CHANNEL, qmin=-8, qmax=7), (2, 19, 56),
+     _x_normal, (2e-3, 2e-2), None),
+    ("int8_tensor_k40", Q(aqfq.INT8, aqfq.PER_TENSOR, qmin=-128, qmax=127), (3, 17, 40),
+     _x_normal, (1e-4, 4e-4), None),
+    ("fp8_head_d24", Q(aqfq.FP8_E4M3, aqfq.PER_HEAD), (53, 5, 24), _x_normal, (2e-5, 2e-4), None),
 ]
 IDS = [c[0] for c in CASES]
 
@@ -132,6 +144,32 @@ def test_scale_grad_accumulate_and_determinism(case):
     ds, dts, _ = gpu_grad(sp, x, dy, scale, ts, want_dx=False, accumulate_from=old)
     got = ds if ds is not None else dts
     assert_grad_close(got, old.astype(np.float64) + r, ra, extra_abs=old, what="accumulated")
+
+
+SIXTEEN = [c for c in CASES if c[0] in ("int8_channel_k512", "int8_channel_k528", "int4_g128",
+                                         "fp8_tensor", "fp8_head", "nvfp4_learned", "nvfp4_dynamic",
+                                         "int8_channel_k24", "fp8_head_d24")]
+
+
+@pytest.mark.parametrize("case", SIXTEEN, ids=[c[0] for c in SIXTEEN])
+def test_sixteen_byte_aligned_views(case):
+    """x, y, dy and dx at addresses that are 16-byte but not 32-byte aligned
+    (a row slice of a wider tensor, for instance): the 128-bit access path
+    gives the same codes, values and gradients as the oracle."""
+    sp = case[1]
+    x, dy, scale, ts = _inputs(case, seed=25)
+    y, c, b = gpu_fwd(sp, x, scale, ts, misalign=True)
+    y_ref, c_ref, b_ref = oracle_fwd(sp, x, scale, ts)
+    assert np.array_equal(y, y_ref) and np.array_equal(c, c_ref)
+    if sp.fmt == aqfq.NVFP4:
+        assert np.array_equal(b, b_ref)
+    ds, dts, dx = gpu_grad(sp, x, dy, scale, ts, misalign=True)
+    ref = oracle_grad(sp, x, dy, scale, ts)
+    if dts is not None:
+        assert_grad_close(dts, ref["dtensor_scale"], ref["dtensor_scale_abs"], what="dtensor_scale")
+    else:
+        assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
+    assert np.array_equal(dx, ref["dx"])
 
 
 @pytest.mark.parametrize("name", ["fp8_tensor", "nvfp4_dynamic"])
@@ -307,11 +345,19 @@ def test_per_head_forward_batch_beyond_grid_limit():
     assert np.array_equal(y, y_ref) and np.array_equal(c, c_ref)
 
 
-@pytest.mark.parametrize("T,H,D", [(300, 8, 64), (97, 5, 48), (1, 3, 16), (2048, 32, 128)])
-def test_observer_and_per_head_scale(T, H, D):
+@pytest.mark.parametrize("T,H,D,misalign", [(300, 8, 64, False), (97, 5, 48, False),
+                                             (1, 3, 16, False), (2048, 32, 128, False),
+                                             (301, 7, 24, False), (203, 4, 8, True),
+                                             (250, 6, 64, True)])
+def test_observer_and_per_head_scale(T, H, D, misalign):
     d = dev()
     x = synth.head_normal_bf16(T, H, D, 0.1, 10.0, seed=70 + T)
-    xd = x.to(d)
+    if misalign:  # 16-byte but not 32-byte aligned
+        buf = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device=d)
+        xd = buf[8:].view(T, H, D)
+        xd.copy_(x)
+    else:
+        xd = x.to(d)
     mn = torch.empty(H, device=d)
     mx = torch.empty(H, device=d)
     aqfq.aqfq_observer_minmax(xd, mn, mx)
@@ -354,8 +400,9 @@ def test_observer_signed_zeros_and_empty():
     assert torch.all(mn == float("inf")) and torch.all(mx == float("-inf"))
 
 
+@pytest.mark.parametrize("misalign", [False, True], ids=["aligned32", "aligned16"])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
-def test_scale_init(case):
+def test_scale_init(case, misalign):
     sp = case[1]
     B, R, K = case[2]
     x = case[3](case[2], 80)
@@ -363,7 +410,13 @@ def test_scale_init(case):
     n = aqfq.scale_numel(sp, B, R, K)
     s = torch.empty(max(n, 1), device=d) if n else None
     ts = torch.empty(B, device=d) if sp.fmt == aqfq.NVFP4 else None
-    aqfq.aqfq_scale_init(sp, x.to(d), s, ts)
+    if misalign:  # 16-byte but not 32-byte aligned
+        buf = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device=d)
+        xd = buf[8:].view(B, R, K)
+        xd.copy_(x)
+    else:
+        xd = x.to(d)
+    aqfq.aqfq_scale_init(sp, xd, s, ts)
     s_ref, ts_ref = oracle.scale_init(ospec(sp), bits(x))
     torch.cuda.synchronize()
     if n:

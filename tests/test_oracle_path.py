@@ -262,6 +262,36 @@ def test_scale_indexing_by_slicing():
                 assert np.array_equal(cs[0, 0], c[b, r, 8 * j:8 * j + 8]) and es[0, 0, 0] == e[b, r, j]
 
 
+def test_rows_of_eight_times_odd_elements():
+    """Rows of K = 8 * odd elements (the library's boundary allows K % 8 == 0):
+    per-channel and per-head QDQ and gradients equal the per-element results of
+    a K % 16 == 0 layout holding the same rows (zero padding changes no other
+    element), codes included; block and group formats reject such K."""
+    B, R, K = 2, 5, 24
+    x = bits(synth.normal_bf16((B, R, K), 0.02, seed=36))
+    dy = bits(synth.normal_bf16((B, R, K), 1.0, seed=37))
+    pad = lambda a: np.concatenate([a, np.zeros((B, R, 8), np.uint16)], axis=2)  # K -> 32
+    for sp, n in [(O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), B * R),
+                  (O.spec(O.INT4, O.PER_CHANNEL, qmin=-8, qmax=7), B * R),
+                  (O.spec(O.FP8_E4M3, O.PER_HEAD), R)]:
+        s = synth.loguniform_f32((n,), 1e-4, 4e-4, seed=38).numpy()
+        if sp.fmt == O.INT4:
+            s = s * 30
+        y, c, _ = O.qdq_fwd(sp, x, s, want_codes=True)
+        yp, cp, _ = O.qdq_fwd(sp, pad(x), s, want_codes=True)
+        assert np.array_equal(y, yp[:, :, :K])
+        assert np.array_equal(c, cp[:, :, :c.shape[2]])
+        g = O.scale_grad(sp, x, dy, s)
+        gp = O.scale_grad(sp, pad(x), pad(dy), s)
+        assert np.array_equal(g["dscale"], gp["dscale"]) and np.array_equal(g["dx"], gp["dx"][:, :, :K])
+    for sp in (O.spec(O.NVFP4, O.PER_GROUP, group=16), O.spec(O.INT4, O.PER_GROUP, group=16, qmin=-8, qmax=7)):
+        with pytest.raises(ValueError):
+            O.qdq_fwd(sp, x, np.ones(B * R * 2, np.float32), np.ones(B, np.float32))
+    with pytest.raises(ValueError):  # not a multiple of 8
+        O.qdq_fwd(O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), x[:, :, :20].copy(),
+                  np.ones(B * R, np.float32))
+
+
 def test_zero_scale_gives_signed_zeros():
     x = bf16_bits_of([1.0, -2.0, 0.0, -0.0] * 4).reshape(1, 1, 16)
     for sp in (O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), O.spec(O.FP8_E4M3, O.PER_TENSOR)):
