@@ -2,7 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload grouped_nvfp4|nvfp4_wa|int4_fp8|observer_fp8|int8_channel|
-                                head_fp8_learned]
+                                head_fp8_learned|grouped_nvfp4_fused|nvfp4_wa_fused|
+                                int8_channel_fused|grouped_nvfp4_gemm|kd_cakld|kd_topk]
 
 One step = one pass of the workload's whole hot path: for the default
 workload (grouped NVFP4 MoE expert stacks, gate_up [128,1536,2048] + down
@@ -213,24 +214,27 @@ def _oracle_jobs(name, inputs):
     def flat(t):
         return t.reshape(-1, t.shape[-1])
 
-    if name == "grouped_nvfp4":
+    if name in ("grouped_nvfp4", "grouped_nvfp4_fused"):
         sp = O.spec(O.NVFP4, O.PER_GROUP, group=16)
-        return [(nm, inputs[nm], inputs[f"dy_{nm}"], sp, 8.75) for nm in ("gate_up", "down")], "experts"
+        bpe = 8.75 if name == "grouped_nvfp4" else 6.5  # separate calls / one pass per stack
+        return [(nm, inputs[nm], inputs[f"dy_{nm}"], sp, bpe) for nm in ("gate_up", "down")], "experts"
     if name == "int4_fp8":
         return [("stack", inputs["stack"], inputs["dy_stack"],
                  O.spec(O.INT4, O.PER_GROUP, group=128, qmin=-8, qmax=7), 4.03125 + 4.0625),
                 ("dense", flat(inputs["dense"]).reshape(-1, 64, 8192),
                  flat(inputs["dy_dense"]).reshape(-1, 64, 8192),
                  O.spec(O.FP8_E4M3, O.PER_CHANNEL), 8.0)], "leading units (expert / 64 rows)"
-    if name == "nvfp4_wa":
+    if name in ("nvfp4_wa", "nvfp4_wa_fused"):
+        fused = name == "nvfp4_wa_fused"
         return [("w", flat(inputs["w"]).reshape(-1, 64, 4096), flat(inputs["dy_w"]).reshape(-1, 64, 4096),
-                 O.spec(O.NVFP4, O.PER_GROUP, group=16), 8.75),
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16), 6.5 if fused else 8.75),
                 ("a", flat(inputs["a"]).reshape(-1, 64, 4096), flat(inputs["dy_a"]).reshape(-1, 64, 4096),
-                 O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK), 10.0)], \
-            "leading units of 64 rows"
-    if name == "int8_channel":
+                 O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK),
+                 8.0 if fused else 10.0)], "leading units of 64 rows"
+    if name in ("int8_channel", "int8_channel_fused"):
         return [("w", flat(inputs["w"]).reshape(-1, 16, 512), flat(inputs["dy"]).reshape(-1, 16, 512),
-                 O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), 8.0)], "leading units of 16 rows"
+                 O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127),
+                 6.0 if name == "int8_channel_fused" else 8.0)], "leading units of 16 rows"
     if name == "grouped_nvfp4_gemm":
         return [("gemm", inputs["w"], None, "gemm", 0.0)], "experts (with their routed rows)"
     if name in ("kd_cakld", "kd_topk"):
@@ -355,6 +359,8 @@ def reference_arm(args):
     from learnable_scale_fake_gb300 import synth, workloads
 
     gen = {"grouped_nvfp4": lambda: synth.cfg3("cpu", 0, experts=8), "nvfp4_wa": lambda: synth.cfg2("cpu"),
+           "grouped_nvfp4_fused": lambda: synth.cfg3("cpu", 0, experts=8),
+           "nvfp4_wa_fused": lambda: synth.cfg2("cpu"), "int8_channel_fused": lambda: synth.cfg1("cpu"),
            "int4_fp8": lambda: synth.cfg4("cpu"), "int8_channel": lambda: synth.cfg1("cpu"),
            "observer_fp8": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0)},
            "head_fp8_learned": lambda: {"act": synth.head_normal_bf16(4096, 32, 128, 0.1, 10.0, 0),
@@ -438,7 +444,8 @@ def main():
         dist.barrier()
     aqfq.lib()
 
-    if args.experts is not None and args.workload in ("grouped_nvfp4", "grouped_nvfp4_gemm"):
+    if args.experts is not None and args.workload in ("grouped_nvfp4", "grouped_nvfp4_fused",
+                                                      "grouped_nvfp4_gemm"):
         wl = workloads.BUILDERS[args.workload](device, experts=args.experts)
     elif args.tokens is not None and args.workload in ("kd_cakld", "kd_topk"):
         wl = workloads.BUILDERS[args.workload](device, tokens=args.tokens)

@@ -188,6 +188,26 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
                             void* dx, int accumulate, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Forward and scale gradient in one pass: y = x_hat exactly as aqfq_qdq_fwd
+ * writes it (no codes) and dscale / dtensor_scale / dx exactly as
+ * aqfq_scale_grad writes them, from one read of x and dy.  For callers that
+ * hold the upstream gradient when they need the forward's output: the
+ * fake-quant forward recomputed in the backward pass (activation
+ * checkpointing), where the weight gradient dW, the fake-quant's upstream
+ * gradient, is formed without x_hat while x_hat is needed for the input
+ * gradient.  x is read once instead of twice and one launch replaces two.
+ * Source: AngelSlim mcore_qad article, sections 1 and 2.3 (forward
+ * fake-quant; the gradient flows to the scale through it).
+ * Arguments as aqfq_scale_grad, plus
+ *   y            device, [batch, rows, K] BF16, required; must not overlap x,
+ *                dy or dx
+ * The workspace is the one aqfq_scale_grad_workspace_bytes gives. */
+aqfq_status aqfq_qdq_fwd_grad(const aqfq_qspec* spec, const void* x, const void* dy,
+                              int64_t batch, int64_t rows, int64_t K, const float* scale,
+                              const float* tensor_scale, void* y, float* dscale,
+                              float* dtensor_scale, void* dx, int accumulate, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* aqfq_scale_grad for callers that cannot allocate device memory (no
  * counterpart in the pages: a library convenience).  Some callers cannot hand
  * over a scratch buffer: a plugin inside a framework that owns all device

@@ -29,7 +29,7 @@ STATUS = {0: "AQFQ_OK", 1: "AQFQ_ERR_NULL", 2: "AQFQ_ERR_SHAPE", 3: "AQFQ_ERR_AL
 
 # every symbol include/aqfq.h declares
 EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_grouped_qdq_gemm", "aqfq_scale_grad",
-           "aqfq_scale_grad_noalloc",
+           "aqfq_qdq_fwd_grad", "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
            "aqfq_scale_init", "aqfq_kd_loss", "aqfq_kd_workspace_bytes",
            "aqfq_selftest_wait_timeout", "aqfq_status_string", "aqfq_version")
@@ -68,6 +68,8 @@ def lib():
                 "aqfq_grouped_qdq": (i32, [S, P, i64, i64, i64, P, P, P, P, P, P]),
                 "aqfq_grouped_qdq_gemm": (i32, [P, P, i64, P, P, P, i64, i64, i64, P, P, P]),
                 "aqfq_scale_grad": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P, sz, P]),
+                "aqfq_qdq_fwd_grad": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, P, i32, P, sz,
+                                            P]),
                 "aqfq_scale_grad_noalloc": (i32, [S, P, P, i64, i64, i64, P, P, P, P, P, i32, P]),
                 "aqfq_scale_grad_workspace_bytes": (sz, [S, i64, i64, i64]),
                 "aqfq_observer_minmax": (i32, [P, i64, i64, i64, P, P, i32, P]),
@@ -217,6 +219,21 @@ def aqfq_scale_grad(spec, x, dy, scale, tensor_scale, dscale=None, dtensor_scale
                                _ptr(tensor_scale), _ptr(dscale), _ptr(dtensor_scale), _ptr(dx),
                                int(bool(accumulate)), _ptr(workspace), wsb, _stream(stream))
     _check("aqfq_scale_grad", st)
+
+
+def aqfq_qdq_fwd_grad(spec, x, dy, scale, tensor_scale, y, dscale=None, dtensor_scale=None,
+                      dx=None, accumulate=False, workspace=None, stream=None):
+    """Forward (y = x_hat) and scale gradient of the same tensor in one pass."""
+    _bf16(x, "x"), _bf16(dy, "dy"), _bf16(dx, "dx"), _bf16(y, "y")
+    _f32(scale, "scale"), _f32(tensor_scale, "tensor_scale")
+    _f32(dscale, "dscale"), _f32(dtensor_scale, "dtensor_scale")
+    B, R, K = _brk(x)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().aqfq_qdq_fwd_grad(ctypes.byref(spec), _ptr(x), _ptr(dy), B, R, K, _ptr(scale),
+                                 _ptr(tensor_scale), _ptr(y), _ptr(dscale), _ptr(dtensor_scale),
+                                 _ptr(dx), int(bool(accumulate)), _ptr(workspace), wsb,
+                                 _stream(stream))
+    _check("aqfq_qdq_fwd_grad", st)
 
 
 def aqfq_scale_grad_noalloc(spec, x, dy, scale, tensor_scale, dscale=None, dtensor_scale=None,

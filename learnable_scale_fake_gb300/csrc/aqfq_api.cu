@@ -206,12 +206,16 @@ size_t aqfq_scale_grad_workspace_bytes(const aqfq_qspec* spec, int64_t batch, in
   return aqfq::grad_workspace_bytes(p);
 }
 
-aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
-                            int64_t rows, int64_t K, const float* scale,
-                            const float* tensor_scale, float* dscale, float* dtensor_scale,
-                            void* dx, int accumulate, void* workspace, size_t workspace_bytes,
-                            void* stream) {
-  Problem p;
+}  // extern "C"
+
+namespace {
+
+// The checks shared by the gradient and the fused forward + gradient: fills p
+// and leaves the launch to the caller.  y (fused only) joins the layout choice.
+aqfq_status check_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
+                       int64_t rows, int64_t K, const float* scale, const float* tensor_scale,
+                       float* dscale, float* dtensor_scale, void* dx, const void* y,
+                       void* workspace, size_t workspace_bytes, Problem& p) {
   aqfq_status s = make_problem(spec, batch, rows, K, p);
   if (s != AQFQ_OK) return s;
   if (p.gran == AQFQ_PER_HEAD && p.rows * int64_t(p.cpr) > (int64_t(1) << 24)) return AQFQ_ERR_SHAPE;
@@ -225,7 +229,7 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
     if (!dscale && scale_count(p) > 0) return AQFQ_ERR_NULL;
     if (dtensor_scale) return AQFQ_ERR_UNSUPPORTED;
   }
-  if ((s = choose_layout(p, {x, dy, dx})) != AQFQ_OK) return s;
+  if ((s = choose_layout(p, {x, dy, dx, y})) != AQFQ_OK) return s;
   if ((dscale && !aligned(dscale, 4)) || (dtensor_scale && !aligned(dtensor_scale, 4)))
     return AQFQ_ERR_ALIGN;
   if (aqfq::sm_count() <= 0) return AQFQ_ERR_CUDA;  // grids and workspace follow the SM count
@@ -235,9 +239,46 @@ aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* d
     if (workspace_bytes < need) return AQFQ_ERR_WORKSPACE;
     if (!aligned(workspace, 8)) return AQFQ_ERR_ALIGN;
   }
+  return AQFQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+aqfq_status aqfq_scale_grad(const aqfq_qspec* spec, const void* x, const void* dy, int64_t batch,
+                            int64_t rows, int64_t K, const float* scale,
+                            const float* tensor_scale, float* dscale, float* dtensor_scale,
+                            void* dx, int accumulate, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  Problem p;
+  aqfq_status s = check_grad(spec, x, dy, batch, rows, K, scale, tensor_scale, dscale,
+                             dtensor_scale, dx, nullptr, workspace, workspace_bytes, p);
+  if (s != AQFQ_OK) return s;
   return finish(aqfq::launch_scale_grad(p, x, dy, scale, tensor_scale, dscale, dtensor_scale, dx,
                                         accumulate, static_cast<double*>(workspace),
                                         static_cast<cudaStream_t>(stream)));
+}
+
+aqfq_status aqfq_qdq_fwd_grad(const aqfq_qspec* spec, const void* x, const void* dy,
+                              int64_t batch, int64_t rows, int64_t K, const float* scale,
+                              const float* tensor_scale, void* y, float* dscale,
+                              float* dtensor_scale, void* dx, int accumulate, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  Problem p;
+  if (!spec) return AQFQ_ERR_NULL;
+  {
+    Problem q;  // y is required whenever there are elements
+    const aqfq_status s0 = make_problem(spec, batch, rows, K, q);
+    if (s0 != AQFQ_OK) return s0;
+    if (!y && elems(q) > 0) return AQFQ_ERR_NULL;
+  }
+  aqfq_status s = check_grad(spec, x, dy, batch, rows, K, scale, tensor_scale, dscale,
+                             dtensor_scale, dx, y, workspace, workspace_bytes, p);
+  if (s != AQFQ_OK) return s;
+  return finish(aqfq::launch_qdq_fwd_grad(p, x, dy, scale, tensor_scale, y, dscale, dtensor_scale,
+                                          dx, accumulate, static_cast<double*>(workspace),
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 aqfq_status aqfq_observer_minmax(const void* x, int64_t T, int64_t H, int64_t D, float* min_out,

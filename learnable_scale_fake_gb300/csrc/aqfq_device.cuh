@@ -440,10 +440,12 @@ __device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[NW], const D
   }
 }
 
-template <int FMT, bool DX, int NW>
+// FWD: also the forward's x_hat of the chunk into yw (the same bits as
+// qdq_chunk_fast: FP grids give |q| * s the sign of x, so -0 stays -0)
+template <int FMT, bool DX, bool FWD = false, int NW>
 __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
                                                  const Divisor& d, const IntRange& r,
-                                                 uint32_t (&dxw)[NW]) {
+                                                 uint32_t (&dxw)[NW], uint32_t* yw = nullptr) {
   float t[2 * NW];
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
@@ -457,12 +459,19 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const
       quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
       term0 = k0 ? q0 : __fsub_rn(q0, v0);
       term1 = k1 ? q1 : __fsub_rn(q1, v1);
+      if constexpr (FWD) yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s));
     } else {
       const uint32_t h = fp_q2<FMT>(v1, v0);
       k0 = fabsf(v0) >= grid_max<FMT>();
       k1 = fabsf(v1) >= grid_max<FMT>();
       term0 = sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : v0);
       term1 = sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : v1);
+      if constexpr (FWD) {
+        const uint32_t a = h & 0x7FFF7FFFu;  // |q| of the pair (f16)
+        yw[i] = pack_bf16x2(__fmul_rn(h2f((uint16_t)(a >> 16)), d.s),
+                            __fmul_rn(h2f((uint16_t)(a & 0xFFFFu)), d.s)) |
+                (xw[i] & 0x80008000u);
+      }
     }
     t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
     t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);

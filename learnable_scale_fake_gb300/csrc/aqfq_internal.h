@@ -38,6 +38,12 @@ cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, c
                               const float* tscale, float* dscale, float* dtscale, void* dx,
                               int accumulate, double* ws, cudaStream_t st);
 
+// forward and scale gradient in one pass (fused.cu); same workspace
+cudaError_t launch_qdq_fwd_grad(const Problem& p, const void* x, const void* dy,
+                                const float* scale, const float* tscale, void* y, float* dscale,
+                                float* dtscale, void* dx, int accumulate, double* ws,
+                                cudaStream_t st);
+
 // statistics (stats.cu)
 cudaError_t launch_observer(const void* x, int64_t T, int64_t H, int64_t D, int lay, float* mn,
                             float* mx, int accumulate, cudaStream_t st);

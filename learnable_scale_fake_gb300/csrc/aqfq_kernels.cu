@@ -1,65 +1,20 @@
 // aqfq_kernels.cu -- fake-quant forward and straight-through scale gradient.
 //
 // Forward (every format and granularity): one streaming kernel.  A CTA of 256
-// threads covers 256*U consecutive 16-element chunks of one batch entry (one
-// expert of a stack, gridDim.y over entries); each lane issues its U 256-bit
-// loads (plus its scale) before computing, then writes one 256-bit BF16 chunk
-// and, on request, its packed codes.  No shared memory, no cross-lane traffic.
+// threads covers 256*U consecutive chunks of one batch entry (one expert of a
+// stack, gridDim.y over entries); each lane issues its U chunk loads (plus
+// its scale) before computing, then writes one BF16 chunk and, on request,
+// its packed codes.  No shared memory, no cross-lane traffic.
 // Source of the operation: AngelSlim mcore_qad article, sections 1, 2.3, 2.4
 // (whole-stack vectorised fake-quant) and 3 (formats).
 //
-// Gradient: the same chunk walk recomputes v and q exactly as the forward,
-// forms dy * (clamped ? q : q - v) per element and reduces it
-//   - per block / group (units of 16..512 elements = 1..32 aligned lanes):
-//     pairwise tree in the lane, xor-butterfly across the unit's lanes, one
-//     store per unit (no atomics, no workspace);
-//   - per channel with long rows: one warp per row, per-lane double
-//     accumulation of chunk sums, double butterfly;
-//   - per tensor / NVFP4 tensor scale: per-CTA double partials into the
-//     caller's workspace; the last CTA to finish (a ticket zeroed on the
-//     stream before the launch) adds them, warp per entry, in fixed order.
-// Every order is fixed, so results are bit-reproducible run to run.
-#include "aqfq_internal.h"
+// Gradient: the kernels of aqfq_grad.cuh, instantiated here without the
+// forward output.
+#include "aqfq_grad.cuh"
 
 namespace aqfq {
 
 namespace {
-
-// Chunks per lane per iteration (U) and minimum resident CTAs per SM asked of
-// the register allocator (MINB), per kernel instantiation, from GB300 sweeps
-// on the five workloads: more resident warps beat deeper per-lane unrolling
-// for the gradient until the register cap starts to spill, which the heavier
-// instantiations (STE input gradient, dynamic block scale, partial sums) do.
-template <int FMT, bool DYN, bool DX, int RED>
-struct GradTune {
-  static constexpr bool heavy = DX || DYN || RED != 0;
-  static constexpr int U = heavy ? 1 : (FMT == F_NVFP4 ? 2 : 3);
-  static constexpr int MINB = heavy ? 1 : (FMT == F_NVFP4 ? 5 : 4);
-};
-template <bool DX>
-struct RowTune {
-  static constexpr int U = 2;
-  static constexpr int MINB = DX ? 1 : 4;
-};
-constexpr int kFwdU = 2;
-
-}  // namespace
-}  // namespace aqfq
-
-namespace aqfq {
-
-namespace {
-
-constexpr int kMaxCtasPerSm = 2048 / kThreads;  // resident 256-thread CTAs per SM, at most
-
-// resident CTAs per SM of a kernel at 256 threads (at least 1)
-template <typename Kernel>
-int occupancy(Kernel kernel) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
-    n = 1;
-  return n;
-}
 
 struct FwdArgs {
   const uint8_t* x;
@@ -131,278 +86,10 @@ __global__ void __launch_bounds__(kThreads) qdq_fwd_kernel(const FwdArgs a) {
   }
 }
 
-struct GradArgs {
-  const uint8_t* x;
-  const uint8_t* dy;
-  uint8_t* dx;
-  const float* scale;
-  const float* tscale;
-  float* dscale;
-  double* ws;           // CTA partials [batch, nparts]
-  unsigned* ticket;     // RED = 1: CTAs done (zeroed by the launch before the kernel)
-  float* red_out;       // RED = 1: the per-batch-entry sums (dscale or the tensor-scale grads)
-  int64_t batch, rows;
-  uint32_t cpb;
-  FastDiv cpr;
-  int lg;
-  IntRange ir;
-  int accumulate;
-  int nparts;
-};
-
-__device__ __forceinline__ void store_grad(float* p, float g, int accumulate) {
-  *p = accumulate ? __fadd_rn(*p, g) : g;
-}
-
-// RED = 0: one scale per aligned run of (1 << lg) lanes, written directly.
-// RED = 1: one scale (or NVFP4 tensor scale) per batch entry, CTA partials.
-template <int FMT, int GRAN, bool DYN, bool DX, int RED, int U, int L>
-__global__ void __launch_bounds__(kThreads, (GradTune<FMT, DYN, DX, RED>::MINB))
-    scale_grad_kernel(const GradArgs a) {
-  constexpr int NW = LayT<L>::NW;
-  const int lane = threadIdx.x & 31;
-  for (int64_t b = blockIdx.y; b < a.batch; b += gridDim.y) {
-    const uint64_t base = (uint64_t)b * a.cpb;
-    float g = 0.0f, st = 0.0f;
-    if constexpr (FMT == F_NVFP4) g = __ldg(a.tscale + b);
-    if constexpr (GRAN == G_TENSOR) st = __ldg(a.scale + b);
-    double acc = 0.0;
-    for (uint64_t c0 = (uint64_t)blockIdx.x * (kThreads * U); c0 < a.cpb;
-         c0 += (uint64_t)gridDim.x * (kThreads * U)) {
-      uint32_t xw[U][NW], dw[U][NW];
-      float sraw[U];
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint64_t c = c0 + j * kThreads + threadIdx.x;
-        sraw[j] = st;
-        if (c < a.cpb) {
-          const uint64_t gc = base + c;
-          ld_chunk<L>(a.x, gc, xw[j]);
-          ld_chunk<L>(a.dy, gc, dw[j]);
-          if constexpr (GRAN == G_GROUP && !DYN) sraw[j] = __ldg(a.scale + (gc >> a.lg));
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint64_t c = c0 + j * kThreads + threadIdx.x;
-        const bool valid = c < a.cpb;
-        const uint64_t gc = base + c;
-        float cs = 0.0f;
-        float dec = 1.0f;
-        if (valid) {
-          float s = sraw[j];
-          if constexpr (FMT == F_NVFP4) {
-            uint32_t ecode;
-            const float sb = DYN ? __fdiv_rn(chunk_amax(xw[j]), 6.0f) : sraw[j];
-            s = nvfp4_block_scale(sb, g, ecode);
-            dec = dec_e4m3x2(ecode).x;
-          }
-          uint32_t dxw[NW];
-          const Divisor dv = make_divisor(s);
-          bool slow = !dv.fast;
-          if (dv.fast) {
-            cs = grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw);
-            slow = isnan(cs);  // a quotient overflowed: redo the chunk exactly
-          }
-          if (slow) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
-          if constexpr (DX) st_chunk<L>(a.dx, gc, dxw);
-        }
-        if constexpr (RED == 0) {
-          const int width = 1 << a.lg;
-          for (int off = 1; off < width; off <<= 1)
-            cs = __fadd_rn(cs, __shfl_xor_sync(0xFFFFFFFFu, cs, off));
-          if (valid && (lane & (width - 1)) == 0) store_grad(a.dscale + (gc >> a.lg), cs, a.accumulate);
-        } else {
-          // NVFP4 dynamic: d S_hat / d g = dec(e_b) with the block code held fixed
-          acc += (double)cs * (double)dec;
-        }
-      }
-    }
-    if constexpr (RED == 1) {
-      __shared__ double red[kThreads / 32];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-      if (lane == 0) red[threadIdx.x >> 5] = acc;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        double t = 0.0;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) t += red[w];
-        a.ws[b * a.nparts + blockIdx.x] = t;
-      }
-      __syncthreads();
-    }
-  }
-  if constexpr (RED == 1) {
-    // the last CTA to finish adds every entry's partials in a fixed order:
-    // warp per entry, lane l takes partials l, l + 32, ..., then a butterfly
-    __shared__ int last;
-    if (threadIdx.x == 0) {
-      __threadfence();  // this CTA's partials before its ticket
-      last = atomicAdd(a.ticket, 1u) == gridDim.x * gridDim.y - 1u;
-    }
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      const volatile double* ws = a.ws;
-      for (int64_t b = threadIdx.x >> 5; b < a.batch; b += kThreads / 32) {
-        double t = 0.0;
-        for (int i = lane; i < a.nparts; i += 32) t += ws[b * a.nparts + i];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-        if (lane == 0) store_grad(a.red_out + b, (float)t, a.accumulate);
-      }
-    }
-  }
-}
-
-// per-channel gradient for rows whose K is not a power of two <= 512: one warp
-// per row, lanes stride over the row's chunks
-template <int FMT, bool DX, int U, int L>
-__global__ void __launch_bounds__(kThreads, (RowTune<DX>::MINB)) scale_grad_row_kernel(const GradArgs a) {
-  constexpr int NW = LayT<L>::NW;
-  const int lane = threadIdx.x & 31;
-  const int64_t nrows = a.batch * a.rows;
-  const uint32_t cpr = a.cpr.d;
-  for (int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); row < nrows;
-       row += (int64_t)gridDim.x * (kThreads / 32)) {
-    const float s = __ldg(a.scale + row);
-    const Divisor dv = make_divisor(s);
-    const uint64_t base = (uint64_t)row * cpr;
-    double acc = 0.0;
-    for (uint32_t c0 = 0; c0 < cpr; c0 += 32 * U) {
-      uint32_t xw[U][NW], dw[U][NW];
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + j * 32 + lane;
-        if (c < cpr) {
-          ld_chunk<L>(a.x, base + c, xw[j]);
-          ld_chunk<L>(a.dy, base + c, dw[j]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + j * 32 + lane;
-        if (c < cpr) {
-          uint32_t dxw[NW];
-          float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[j], dw[j], dv, a.ir, dxw) : 0.0f;
-          if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[j], dw[j], s, a.ir, dxw);
-          acc += (double)cs;
-          if constexpr (DX) st_chunk<L>(a.dx, base + c, dxw);
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    if (lane == 0) store_grad(a.dscale + row, (float)acc, a.accumulate);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// per-head gradient: x [T, H, D], one scale per head shared by all tokens.
-// The threads used are a multiple of the chunks per token (cpt), so thread j
-// always reads column-chunk j % cpt (one head) of successive tokens and sums
-// its chunk gradients in double; ws[j] holds that partial.  A second kernel
-// adds each head's partials in a fixed order.
-// ---------------------------------------------------------------------------
-struct HeadArgs {
-  const uint8_t* x;
-  const uint8_t* dy;
-  uint8_t* dx;
-  const float* scale;
-  double* ws;
-  uint64_t nchunks;  // T * cpt
-  uint32_t cpt;
-  FastDiv cph;       // chunks per head
-  uint64_t used;     // threads with work (multiple of cpt)
-  IntRange ir;
-};
-
-template <int FMT, bool DX, int L>
-__global__ void __launch_bounds__(kThreads) scale_grad_head_kernel(const HeadArgs a) {
-  constexpr int NW = LayT<L>::NW;
-  const uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-  if (j >= a.used) return;
-  const float s = __ldg(a.scale + fdiv((uint32_t)(j % a.cpt), a.cph));
-  const Divisor dv = make_divisor(s);
-  double acc = 0.0;
-  for (uint64_t c0 = j; c0 < a.nchunks; c0 += 2 * a.used) {
-    uint32_t xw[2][NW], dw[2][NW];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint64_t c = c0 + u * a.used;
-      if (c < a.nchunks) {
-        ld_chunk<L>(a.x, c, xw[u]);
-        ld_chunk<L>(a.dy, c, dw[u]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint64_t c = c0 + u * a.used;
-      if (c >= a.nchunks) continue;
-      uint32_t dxw[NW];
-      float cs = dv.fast ? grad_chunk_fast<FMT, DX>(xw[u], dw[u], dv, a.ir, dxw) : 0.0f;
-      if (!dv.fast || isnan(cs)) cs = grad_chunk<FMT, DX>(xw[u], dw[u], s, a.ir, dxw);
-      acc += (double)cs;
-      if constexpr (DX) st_chunk<L>(a.dx, c, dxw);
-    }
-  }
-  a.ws[j] = acc;
-}
-
-// dscale[h] = sum over r < used / cpt, c < cph of ws[r * cpt + h * cph + c]
-__global__ void reduce_heads_kernel(const double* ws, uint64_t rounds, uint32_t cpt, uint32_t cph,
-                                    int64_t H, float* out, int accumulate) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t h = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); h < H;
-       h += (int64_t)gridDim.x * (blockDim.x / 32)) {
-    double t = 0.0;
-    const uint64_t n = rounds * cph;
-    for (uint64_t i = lane; i < n; i += 32) t += ws[(i / cph) * cpt + h * cph + (i % cph)];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-    if (lane == 0) store_grad(out + h, (float)t, accumulate);
-  }
-}
-
-// threads used by the per-head gradient: one wave of `ctas_per_sm` CTAs per
-// SM, rounded down to a multiple of the chunks per token (at least one token's
-// worth), and no more than the chunks there are
-uint64_t head_threads(const Problem& p, int ctas_per_sm) {
-  const uint64_t cpt = p.cpr * uint64_t(p.rows);
-  const uint64_t nchunks = uint64_t(p.batch) * cpt;
-  if (cpt == 0) return 0;
-  uint64_t want = uint64_t(sm_count()) * ctas_per_sm * kThreads;
-  uint64_t used = want / cpt * cpt;
-  if (used < cpt) used = cpt;
-  if (used > nchunks) used = nchunks;
-  return used;
-}
-
-// ---------------------------------------------------------------------------
-// host-side dispatch
-// ---------------------------------------------------------------------------
-
-int log2_exact(int64_t v) {
-  int l = 0;
-  while ((int64_t(1) << l) < v) ++l;
-  return (int64_t(1) << l) == v ? l : -1;
-}
-
-dim3 stream_grid(uint32_t cpb, int64_t batch, int U, int cap) {
-  uint64_t gx = (uint64_t(cpb) + uint64_t(kThreads) * U - 1) / (uint64_t(kThreads) * U);
-  if (gx < 1) gx = 1;
-  if (cap > 0 && gx > uint64_t(cap)) gx = cap;
-  if (gx > 0x7FFFFFFFull) gx = 0x7FFFFFFFull;
-  uint64_t gy = batch < 65535 ? uint64_t(batch) : 65535ull;
-  if (gy < 1) gy = 1;
-  return dim3((unsigned)gx, (unsigned)gy, 1);
-}
-
 template <int FMT, int GRAN, bool DYN, bool CODES, int L>
 void fwd_launch(const FwdArgs& a, cudaStream_t st) {
   constexpr int U = kFwdU;
-  if (U > 1 && a.cpb >= uint32_t(U) * kThreads) {
+  if (U > 1 && grad_unroll(a.cpb, a.batch, U) == U) {
     qdq_fwd_kernel<FMT, GRAN, DYN, CODES, U, L>
         <<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
   } else {
@@ -452,102 +139,6 @@ void fwd_lay(const Problem& p, const FwdArgs& a, cudaStream_t st) {
   }
 }
 
-// unroll actually used by a gradient launch (U of the traits, or 1 when the
-// batch entry has fewer than U * 256 chunks)
-int grad_unroll(uint32_t cpb, int U) { return cpb >= uint32_t(U) * kThreads ? U : 1; }
-
-bool grad_needs_partials(const Problem& p) {
-  return (p.fmt == F_NVFP4 && p.mode == 1) || (p.fmt != F_NVFP4 && p.gran == G_TENSOR);
-}
-
-// every partial-sum (RED = 1) instantiation is "heavy": U = 1
-static_assert(GradTune<F_NVFP4, true, false, 1>::U == 1 && GradTune<F_FP8, false, false, 1>::U == 1,
-              "partial-sum kernels are launched with one chunk per lane");
-// CTAs per batch entry of a partial-sum launch: one wave over all entries
-// (ctas_per_sm resident CTAs on every SM), at most one per 256 chunks
-int grad_parts(const Problem& p, int ctas_per_sm) {
-  const int64_t entries = p.batch < 65535 ? p.batch : 65535;
-  int64_t parts = int64_t(sm_count()) * ctas_per_sm / (entries > 0 ? entries : 1);
-  const int64_t need = (int64_t(p.cpb) + kThreads - 1) / kThreads;
-  if (parts > need) parts = need;
-  if (parts < 1) parts = 1;
-  return (int)parts;
-}
-
-// block-path lanes per unit (log2), or -1 when the row kernel is needed
-int grad_unit_lg(const Problem& p) {
-  if (p.fmt == F_NVFP4) return 0;
-  if (p.gran == G_GROUP) return log2_exact(p.group / 16);
-  if (p.gran == G_ROW) {
-    const int l = log2_exact(p.cpr);
-    return (l >= 0 && l <= 5) ? l : -1;
-  }
-  return 0;
-}
-
-// returns the CTAs per batch entry of a partial-sum launch (0 otherwise)
-template <int FMT, int GRAN, bool DYN, bool DX, int RED, int L>
-int grad_launch(const Problem& p, GradArgs a, cudaStream_t st) {
-  constexpr int U = GradTune<FMT, DYN, DX, RED>::U;
-  if constexpr (RED == 1) {
-    auto k = scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1, L>;
-    a.nparts = grad_parts(p, occupancy(k));
-    k<<<stream_grid(a.cpb, a.batch, 1, a.nparts), kThreads, 0, st>>>(a);
-    return a.nparts;
-  } else {
-    if (U > 1 && grad_unroll(a.cpb, U) == U) {
-      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, U, L>
-          <<<stream_grid(a.cpb, a.batch, U, 0), kThreads, 0, st>>>(a);
-    } else {
-      scale_grad_kernel<FMT, GRAN, DYN, DX, RED, 1, L>
-          <<<stream_grid(a.cpb, a.batch, 1, 0), kThreads, 0, st>>>(a);
-    }
-    return 0;
-  }
-}
-
-template <int FMT, bool DX, int L>
-int grad_dispatch(const Problem& p, GradArgs a, cudaStream_t st) {
-  if constexpr (FMT == F_NVFP4) {
-    static_assert(L != L_8, "NVFP4 blocks are 16 elements");
-    if (p.mode == 1) return grad_launch<FMT, G_GROUP, true, DX, 1, L>(p, a, st);
-    return grad_launch<FMT, G_GROUP, false, DX, 0, L>(p, a, st);
-  } else {
-    if (p.gran == G_TENSOR) {
-      return grad_launch<FMT, G_TENSOR, false, DX, 1, L>(p, a, st);
-    } else if (a.lg >= 0) {  // per-group, or per-channel rows of 1..32 chunks (power of two)
-      return grad_launch<FMT, G_GROUP, false, DX, 0, L>(p, a, st);
-    } else {
-      const int64_t nrows = p.batch * p.rows;
-      int64_t blocks = (nrows + kThreads / 32 - 1) / (kThreads / 32);
-      if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-      if (blocks < 1) blocks = 1;
-      scale_grad_row_kernel<FMT, DX, RowTune<DX>::U, L><<<(unsigned)blocks, kThreads, 0, st>>>(a);
-      return 0;
-    }
-  }
-}
-
-template <int FMT, int L>
-int grad_dx(const Problem& p, const GradArgs& a, cudaStream_t st) {
-  if (a.dx) return grad_dispatch<FMT, true, L>(p, a, st);
-  return grad_dispatch<FMT, false, L>(p, a, st);
-}
-
-template <int FMT>
-int grad_fmt(const Problem& p, const GradArgs& a, cudaStream_t st) {
-  if constexpr (FMT == F_NVFP4) {
-    if (p.lay == L_32) return grad_dx<FMT, L_32>(p, a, st);
-    return grad_dx<FMT, L_16>(p, a, st);
-  } else {
-    switch (p.lay) {
-      case L_32: return grad_dx<FMT, L_32>(p, a, st);
-      case L_16: return grad_dx<FMT, L_16>(p, a, st);
-      default: return grad_dx<FMT, L_8>(p, a, st);
-    }
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_qdq_fwd(const Problem& p, const void* x, const float* scale,
@@ -587,116 +178,11 @@ size_t grad_workspace_bytes(const Problem& p) {
   return 16 + size_t(p.batch) * size_t(grad_parts(p, kMaxCtasPerSm)) * sizeof(double);
 }
 
-namespace {
-
-// returns the threads used (one wave of the kernel's resident CTAs)
-template <int FMT, bool DX, int L>
-uint64_t head_launch(const Problem& p, HeadArgs a, cudaStream_t st) {
-  auto k = scale_grad_head_kernel<FMT, DX, L>;
-  a.used = head_threads(p, occupancy(k));
-  const uint64_t blocks = (a.used + kThreads - 1) / kThreads;
-  k<<<(unsigned)blocks, kThreads, 0, st>>>(a);
-  return a.used;
-}
-
-template <int FMT, int L>
-uint64_t head_dx(const Problem& p, const HeadArgs& a, cudaStream_t st) {
-  if (a.dx) return head_launch<FMT, true, L>(p, a, st);
-  return head_launch<FMT, false, L>(p, a, st);
-}
-
-template <int FMT>
-uint64_t head_fmt(const Problem& p, const HeadArgs& a, cudaStream_t st) {
-  switch (p.lay) {
-    case L_32: return head_dx<FMT, L_32>(p, a, st);
-    case L_16: return head_dx<FMT, L_16>(p, a, st);
-    default: return head_dx<FMT, L_8>(p, a, st);
-  }
-}
-
-cudaError_t launch_head_grad(const Problem& p, const void* x, const void* dy, const float* scale,
-                             float* dscale, void* dx, int accumulate, double* ws,
-                             cudaStream_t st) {
-  if (p.rows == 0) return cudaSuccess;
-  if (p.batch == 0 || p.cpr == 0) {  // no elements: every head's gradient is an empty sum
-    if (!accumulate) return cudaMemsetAsync(dscale, 0, size_t(p.rows) * sizeof(float), st);
-    return cudaSuccess;
-  }
-  HeadArgs a;
-  a.x = static_cast<const uint8_t*>(x);
-  a.dy = static_cast<const uint8_t*>(dy);
-  a.dx = static_cast<uint8_t*>(dx);
-  a.scale = scale;
-  a.ws = ws;
-  a.cpt = p.cpr * uint32_t(p.rows);
-  a.nchunks = uint64_t(p.batch) * a.cpt;
-  a.cph = make_fastdiv(p.cpr);
-  a.used = 0;
-  a.ir = IntRange{p.qmin, p.qmax};
-  uint64_t used;
-  switch (p.fmt) {
-    case F_INT8: used = head_fmt<F_INT8>(p, a, st); break;
-    case F_INT4: used = head_fmt<F_INT4>(p, a, st); break;
-    default: used = head_fmt<F_FP8>(p, a, st); break;
-  }
-  int64_t blocks = (p.rows + 7) / 8;
-  if (blocks > 65535) blocks = 65535;
-  reduce_heads_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, used / a.cpt, a.cpt, p.cpr, p.rows,
-                                                        dscale, accumulate);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_scale_grad(const Problem& p, const void* x, const void* dy, const float* scale,
                               const float* tscale, float* dscale, float* dtscale, void* dx,
                               int accumulate, double* ws, cudaStream_t st) {
-  if (p.fmt != F_NVFP4 && p.gran == G_HEAD)
-    return launch_head_grad(p, x, dy, scale, dscale, dx, accumulate, ws, st);
-  const bool partials = grad_needs_partials(p);
-  float* out = (p.fmt == F_NVFP4 && p.mode == 1) ? dtscale : dscale;
-  if (p.batch == 0) return cudaSuccess;
-  if (p.cpb == 0) {
-    // empty rows: every gradient is an empty sum
-    if (!accumulate) {
-      size_t n = partials ? size_t(p.batch)
-                          : (p.gran == G_ROW ? size_t(p.batch * p.rows) : 0);
-      if (n) {
-        cudaError_t e = cudaMemsetAsync(out, 0, n * sizeof(float), st);
-        if (e != cudaSuccess) return e;
-      }
-    }
-    return cudaGetLastError();
-  }
-  GradArgs a;
-  a.x = static_cast<const uint8_t*>(x);
-  a.dy = static_cast<const uint8_t*>(dy);
-  a.dx = static_cast<uint8_t*>(dx);
-  a.scale = scale;
-  a.tscale = tscale;
-  a.dscale = dscale;
-  a.ws = partials ? ws + 2 : ws;  // after the 16-byte ticket header
-  a.ticket = partials ? reinterpret_cast<unsigned*>(ws) : nullptr;
-  a.red_out = out;
-  a.batch = p.batch;
-  a.rows = p.rows;
-  a.cpb = p.cpb;
-  a.cpr = make_fastdiv(p.cpr);
-  a.lg = grad_unit_lg(p);
-  a.ir = IntRange{p.qmin, p.qmax};
-  a.accumulate = accumulate;
-  a.nparts = 0;
-  if (partials) {  // the ticket starts at zero on the stream, before the kernel
-    cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);
-    if (e != cudaSuccess) return e;
-  }
-  switch (p.fmt) {
-    case F_INT8: grad_fmt<F_INT8>(p, a, st); break;
-    case F_INT4: grad_fmt<F_INT4>(p, a, st); break;
-    case F_FP8: grad_fmt<F_FP8>(p, a, st); break;
-    default: grad_fmt<F_NVFP4>(p, a, st); break;
-  }
-  return cudaGetLastError();
+  return launch_grad<false>(p, x, dy, scale, tscale, dscale, dtscale, dx, nullptr, accumulate, ws,
+                            st);
 }
 
 }  // namespace aqfq

@@ -19,6 +19,9 @@ step of its hot path with each call's algorithmic bytes:
                  (Qwen3-sized vocabulary), cakld over the whole vocabulary,
                  with the student-logit gradient
   kd_topk        the same with forward KL over the teacher's top-1000 tokens
+  *_fused        grouped_nvfp4 / nvfp4_wa / int8_channel with forward and
+                 scale gradient of each tensor in one aqfq_qdq_fwd_grad pass
+                 (the forward recomputed in the backward pass)
 
 Algorithmic bytes count what the call must move once: inputs read, outputs
 written (no codes: the steps do not request them).
@@ -186,6 +189,15 @@ CONFIGS = {
     "grouped_nvfp4_gemm": {"workload": "grouped_nvfp4_gemm_gate_up", "x": [65536, 2048],
                            "w": [128, 1536, 2048],
                            "routing": "multinomial, expert popularity exp(N(0,0.3^2))"},
+    "grouped_nvfp4_fused": {"workload": "grouped_nvfp4_moe_stacks_fused_fwd_grad",
+                            "gate_up": [128, 1536, 2048], "down": [128, 2048, 768],
+                            "format": "nvfp4 (e2m1, 16-elem blocks, e4m3 block scale, fp32 tensor scale)",
+                            "values": "student-t(4)*0.02, 0.05% outliers x20",
+                            "scale_init": "amax/6, amax/2688", "fused": "aqfq_qdq_fwd_grad per stack"},
+    "nvfp4_wa_fused": {"workload": "nvfp4_weight_activation_fused_fwd_grad", "w": [4096, 4096],
+                       "a": [8192, 4096], "fused": "aqfq_qdq_fwd_grad per tensor"},
+    "int8_channel_fused": {"workload": "int8_per_channel_weight_fused_fwd_grad", "w": [256, 512],
+                           "fused": "aqfq_qdq_fwd_grad"},
     "kd_cakld": {"workload": "kd_cakld_logits", "logits": [synth.KD_TOKENS, synth.KD_VOCAB],
                  "loss": "cakld", "topk": 0},
     "kd_topk": {"workload": "kd_kl_top1000_logits", "logits": [synth.KD_TOKENS, synth.KD_VOCAB],
@@ -342,6 +354,90 @@ def int8_channel(dev, seed=0):
     return wl
 
 
+def _fused(wl, name, sp, x, dy, s, g, dx=None, ws=None, dyn=False):
+    """One aqfq_qdq_fwd_grad call on x: y, the scale gradient (and dx), from one
+    read of x and dy.  Returns the outputs."""
+    y = torch.empty_like(x)
+    n = x.numel()
+    ns = 0 if s is None else s.numel()
+    if dyn:
+        dg = torch.empty_like(g)
+        kw = {"dtensor_scale": dg}
+        outs = {f"y_{name}": y, f"dtscale_{name}": dg}
+    else:
+        ds = torch.empty_like(s)
+        kw = {"dscale": ds}
+        outs = {f"y_{name}": y, f"dscale_{name}": ds}
+    if dx is not None:
+        outs[f"dx_{name}"] = dx
+    nbytes = 6 * n + 8 * ns + (2 * n if dx is not None else 0)  # x, dy, y (+dx); S read, dS written
+    wl.ops.append(Op(f"qdq_fwd_grad {name}", "fused_fwd_grad", n, nbytes,
+                     lambda st: aqfq.aqfq_qdq_fwd_grad(sp, x, dy, s, g, y, dx=dx, workspace=ws,
+                                                       stream=st, **kw),
+                     2 if ws is not None else 1))
+    wl.outputs.update(outs)
+
+
+def grouped_nvfp4_fused(dev, seed=0, experts=None):
+    """The grouped NVFP4 expert stacks with forward and scale gradient of each
+    stack in one pass (aqfq_qdq_fwd_grad): the forward recomputed in the
+    backward pass."""
+    d = synth.cfg3(dev, seed, experts)
+    wl = Workload("grouped_nvfp4_fused",
+                  "grouped NVFP4 MoE expert stacks, fused QDQ fwd + per-block scale grad per stack",
+                  dict(CONFIGS["grouped_nvfp4_fused"], gate_up=list(d["gate_up"].shape),
+                       down=list(d["down"].shape)))
+    sp = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16)
+    for nm in ("gate_up", "down"):
+        w, dy = d[nm], d[f"dy_{nm}"]
+        E, N, K = w.shape
+        s = torch.empty(E * N * K // 16, device=dev)
+        g = torch.empty(E, device=dev)
+        aqfq.aqfq_scale_init(sp, w, s, g)
+        _fused(wl, nm, sp, w, dy, s, g)
+        wl.inputs.update({nm: w, f"dy_{nm}": dy, f"scale_{nm}": s, f"tscale_{nm}": g})
+    return wl
+
+
+def nvfp4_wa_fused(dev, seed=0):
+    """NVFP4 weight [4096,4096] and activations [8192,4096] with forward and
+    scale gradient of each tensor in one pass (the activation with its STE
+    input gradient)."""
+    d = synth.cfg2(dev, seed)
+    wl = Workload("nvfp4_wa_fused", "NVFP4 weight + activations, fused fwd + scale grad per tensor",
+                  dict(CONFIGS["nvfp4_wa_fused"]))
+    sp = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16)
+    w, dyw = d["w"].unsqueeze(0), d["dy_w"].unsqueeze(0)
+    s = torch.empty(w.numel() // 16, device=dev)
+    g = torch.empty(1, device=dev)
+    aqfq.aqfq_scale_init(sp, w, s, g)
+    _fused(wl, "w", sp, w, dyw, s, g)
+    spd = Q(aqfq.NVFP4, aqfq.PER_GROUP, group=16, mode=aqfq.SCALE_DYNAMIC_BLOCK)
+    a, dya = d["a"].unsqueeze(0), d["dy_a"].unsqueeze(0)
+    ga = torch.empty(1, device=dev)
+    aqfq.aqfq_scale_init(spd, a, None, ga)
+    ws = torch.empty(max(1, aqfq.aqfq_scale_grad_workspace_bytes(spd, *a.shape) // 8),
+                     dtype=torch.float64, device=dev)
+    _fused(wl, "a", spd, a, dya, None, ga, dx=torch.empty_like(a), ws=ws, dyn=True)
+    wl.inputs.update({"w": w, "dy_w": dyw, "scale_w": s, "tscale_w": g, "a": a, "dy_a": dya,
+                      "tscale_a": ga})
+    return wl
+
+
+def int8_channel_fused(dev, seed=0):
+    """INT8 per-channel weight [256,512]: forward and scale gradient in one launch."""
+    d = synth.cfg1(dev, seed)
+    w, dy = d["w"].unsqueeze(0), d["dy"].unsqueeze(0)
+    sp = Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127)
+    s = torch.empty(w.shape[1], device=dev)
+    aqfq.aqfq_scale_init(sp, w, s, None)
+    wl = Workload("int8_channel_fused", "INT8 per-channel weight [256,512], fused fwd + scale grad",
+                  dict(CONFIGS["int8_channel_fused"]))
+    _fused(wl, "w", sp, w, dy, s, None)
+    wl.inputs.update({"w": w, "dy": dy, "scale": s})
+    return wl
+
+
 def grouped_nvfp4_gemm(dev, seed=0, tokens=8192, topk=8, experts=None):
     """MoE gate_up projection with NVFP4 fake-quantized expert weights (nvfp4a16):
     routed activations X [tokens * topk, 2048] grouped by expert, W [128, 1536, 2048].
@@ -446,7 +542,9 @@ def kd_topk(dev, seed=0, tokens=synth.KD_TOKENS):
     return _kd("kd_topk", aqfq.KD_KL, 1000, dev, seed, T=tokens)
 
 
-BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
+BUILDERS = {"grouped_nvfp4": grouped_nvfp4, "grouped_nvfp4_fused": grouped_nvfp4_fused,
+            "nvfp4_wa_fused": nvfp4_wa_fused, "int8_channel_fused": int8_channel_fused,
+            "nvfp4_wa": nvfp4_wa, "int4_fp8": int4_fp8,
             "observer_fp8": observer_fp8, "int8_channel": int8_channel,
             "head_fp8_learned": head_fp8_learned, "grouped_nvfp4_gemm": grouped_nvfp4_gemm,
             "kd_cakld": kd_cakld, "kd_topk": kd_topk}

@@ -146,6 +146,45 @@ def gpu_grad(sp, x, dy, scale, ts, want_dx=True, accumulate_from=None, misalign=
             None if dx is None else bits(dx))
 
 
+def gpu_fwd_grad(sp, x, dy, scale, ts, want_dx=True, misalign=False):
+    """The fused forward + gradient on the GPU (guard-banded outputs); returns
+    numpy (y bits, dscale, dtensor_scale, dx bits)."""
+    d = dev()
+    x3, dy3 = as3(x), as3(dy)
+    B, R, K = x3.shape
+    xd, dyd = on_device(x3, misalign), on_device(dy3, misalign)
+    sd = None if scale is None else scale.to(d)
+    td = None if ts is None else ts.to(d)
+    dyn = sp.fmt == aqfq.NVFP4 and sp.mode == aqfq.SCALE_DYNAMIC_BLOCK
+    n = B * R * K
+    ga = 72 if misalign else 64
+    y, yw = guarded(n, torch.bfloat16, d, ga)
+    y = y.view(B, R, K)
+    n_s = aqfq.scale_numel(sp, B, R, K)
+    ds = dts = None
+    if dyn:
+        dts, dtw = guarded(B, torch.float32, d, 16)
+    else:
+        ds, dsw = guarded(n_s, torch.float32, d, 16)
+    dx = dxw = None
+    if want_dx:
+        dx, dxw = guarded(n, torch.bfloat16, d, ga)
+        dx = dx.view(B, R, K)
+    wsb = aqfq.aqfq_scale_grad_workspace_bytes(sp, B, R, K)
+    ws = torch.empty(max(wsb // 8, 1), dtype=torch.float64, device=d) if wsb else None
+    aqfq.aqfq_qdq_fwd_grad(sp, xd, dyd, sd, td, y, dscale=ds, dtensor_scale=dts, dx=dx, workspace=ws)
+    torch.cuda.synchronize()
+    assert canaries_intact(yw, n, ga), "write outside y"
+    if dyn:
+        assert canaries_intact(dtw, B, 16)
+    else:
+        assert canaries_intact(dsw, n_s, 16)
+    if want_dx:
+        assert canaries_intact(dxw, n, ga)
+    return (bits(y), None if ds is None else ds.cpu().numpy(), None if dts is None else dts.cpu().numpy(),
+            None if dx is None else bits(dx))
+
+
 def oracle_fwd(sp, x, scale, ts):
     return oracle.qdq_fwd(ospec(sp), bits(as3(x)), None if scale is None else scale.numpy(),
                           None if ts is None else ts.numpy(), True)

@@ -119,6 +119,26 @@ def test_grad_argument_checks(L):
     assert aqfq.aqfq_scale_grad_workspace_bytes(NV, 1, 4, 40) == 0  # rejected shape
 
 
+def fused(L, spec, x=A, dy=2 * A, B=1, R=4, K=64, scale=A, ts=A, y=4 * A, ds=3 * A, dts=None,
+          dx=None, ws=None, wsb=0):
+    return L.aqfq_qdq_fwd_grad(ctypes.byref(spec), x, dy, B, R, K, scale, ts, y, ds, dts, dx, 0, ws,
+                               wsb, None)
+
+
+def test_fused_argument_checks(L):
+    """aqfq_qdq_fwd_grad checks what aqfq_scale_grad checks, plus y."""
+    assert L.aqfq_qdq_fwd_grad(None, A, A, 1, 4, 64, A, A, A, A, None, None, 0, None, 0, None) == NULL
+    assert fused(L, NV, y=None) == NULL
+    assert fused(L, NV, y=4 * A + 8) == ALIGN
+    assert fused(L, NV, ds=None) == NULL
+    assert fused(L, NV, dts=A) == UNSUP
+    assert fused(L, NV, K=24) == SHAPE
+    assert fused(L, NV, dy=A + 8) == ALIGN
+    assert fused(L, I8, K=20) == SHAPE
+    # an empty tensor needs no buffers
+    assert fused(L, NV, B=0, x=None, dy=None, y=None, ds=None, ts=None) in (OK, CUDA)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers pass the checks: no device only")
 def test_boundary_accepts_rows_of_eight_and_sixteen_byte_alignment(L):
     """K % 8 == 0 rows (per-tensor / per-channel / per-head INT8, INT4, FP8) and
@@ -138,6 +158,8 @@ def test_boundary_accepts_rows_of_eight_and_sixteen_byte_alignment(L):
     assert grad(L, NV, x=A + 16, dy=A + 48) == CUDA_
     assert L.aqfq_observer_minmax(A + 16, 4, 2, 24, A, 2 * A, 0, None) == CUDA_
     assert L.aqfq_scale_init(ctypes.byref(I8), A + 16, 1, 4, 24, A, None, None) == CUDA_
+    assert fused(L, I8, K=24, y=4 * A + 16) == CUDA_
+    assert fused(L, NVD, scale=None, ds=None, dts=A, ws=5 * A, wsb=1 << 20) == CUDA_
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a device")

@@ -75,6 +75,35 @@ def test_grouped_nvfp4_stacks_full_size():
         gc.collect()
 
 
+def test_fused_workloads_full_size():
+    """The fused forward + gradient workloads (one aqfq_qdq_fwd_grad pass per
+    tensor) at the bench's sizes: every expert of both NVFP4 stacks, the NVFP4
+    weight and activation tensors (with dx), the INT8 per-channel weight."""
+    osp = O.spec(O.NVFP4, O.PER_GROUP, group=16)
+    wl = workloads.grouped_nvfp4_fused(dev())
+    _run(wl)
+    for nm in ("gate_up", "down"):
+        _check_block(osp, bits(wl.inputs[nm]), bits(wl.inputs[f"dy_{nm}"]),
+                     _f32(wl.inputs[f"scale_{nm}"]), _f32(wl.inputs[f"tscale_{nm}"]),
+                     bits(wl.outputs[f"y_{nm}"]), _f32(wl.outputs[f"dscale_{nm}"]))
+        gc.collect()
+    del wl
+    gc.collect()
+    wl = workloads.nvfp4_wa_fused(dev())
+    _run(wl)
+    _check_block(osp, bits(wl.inputs["w"]), bits(wl.inputs["dy_w"]), _f32(wl.inputs["scale_w"]),
+                 _f32(wl.inputs["tscale_w"]), bits(wl.outputs["y_w"]), _f32(wl.outputs["dscale_w"]))
+    osd = O.spec(O.NVFP4, O.PER_GROUP, group=16, mode=O.SCALE_DYNAMIC_BLOCK)
+    _check_block(osd, bits(wl.inputs["a"]), bits(wl.inputs["dy_a"]), None, _f32(wl.inputs["tscale_a"]),
+                 bits(wl.outputs["y_a"]), None, dts_gpu=_f32(wl.outputs["dtscale_a"]),
+                 dx_gpu=bits(wl.outputs["dx_a"]))
+    wl = workloads.int8_channel_fused(dev())
+    _run(wl)
+    _check_block(O.spec(O.INT8, O.PER_CHANNEL, qmin=-128, qmax=127), bits(wl.inputs["w"]),
+                 bits(wl.inputs["dy"]), _f32(wl.inputs["scale"]), None, bits(wl.outputs["y_w"]),
+                 _f32(wl.outputs["dscale_w"]))
+
+
 def test_nvfp4_weight_and_activation_full_size():
     wl = workloads.nvfp4_wa(dev())
     _run(wl)

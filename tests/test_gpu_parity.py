@@ -8,8 +8,8 @@ import torch
 
 import oracle
 from learnable_scale_fake_gb300 import aqfq, synth
-from paritylib import (as3, assert_grad_close, bits, dev, gpu_fwd, gpu_grad, oracle_fwd,
-                       oracle_grad, ospec)
+from paritylib import (as3, assert_grad_close, bits, dev, gpu_fwd, gpu_fwd_grad, gpu_grad,
+                       oracle_fwd, oracle_grad, ospec)
 
 pytestmark = pytest.mark.gpu
 
@@ -121,6 +121,30 @@ def test_scale_grad(case):
         frac = assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
         print(f"{case[0]}: {frac:.4f} of units within plain 1e-5 relative")
     assert np.array_equal(dx, ref["dx"]), f"{np.count_nonzero(dx != ref['dx'])} dx mismatches"
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_fused_forward_and_gradient(case):
+    """aqfq_qdq_fwd_grad: one pass writes the forward's x_hat (bit-exact) and
+    the scale gradient (within the tolerance) and dx (bit-exact), as the two
+    separate entry points do; 16-byte aligned views for every third case."""
+    sp = case[1]
+    x, dy, scale, ts = _inputs(case, seed=5)
+    mis = IDS.index(case[0]) % 3 == 0
+    y, ds, dts, dx = gpu_fwd_grad(sp, x, dy, scale, ts, misalign=mis)
+    y_ref, _, _ = oracle_fwd(sp, x, scale, ts)
+    ref = oracle_grad(sp, x, dy, scale, ts)
+    assert np.array_equal(y, y_ref), f"{np.count_nonzero(y != y_ref)} x_hat mismatches"
+    if dts is not None:
+        assert_grad_close(dts, ref["dtensor_scale"], ref["dtensor_scale_abs"], what="dtensor_scale")
+    else:
+        assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
+    assert np.array_equal(dx, ref["dx"])
+    # without the STE input gradient: the same x_hat and scale gradient
+    y2, ds2, dts2, _ = gpu_fwd_grad(sp, x, dy, scale, ts, want_dx=False)
+    assert np.array_equal(y2, y_ref)
+    got, want = (ds2, ds) if ds is not None else (dts2, dts)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), "not reproducible"
 
 
 ACC = [c for c in CASES if c[0] in ("int8_channel_k512", "int4_g128", "fp8_tensor", "fp8_head",
@@ -236,6 +260,10 @@ def test_special_values():
         ref = oracle_grad(sp, x, dy, s, ts)
         assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
         assert np.array_equal(dx, ref["dx"])
+        # the fused pass gives the same x_hat and gradients on these values too
+        yf, dsf, _, dxf = gpu_fwd_grad(sp, x, dy, s, ts)
+        assert np.array_equal(yf, y_ref) and np.array_equal(dxf, ref["dx"])
+        assert_grad_close(dsf, ref["dscale"], ref["dscale_abs"])
     # scales at and beyond the ends of the reciprocal fast path [2^-64, 2^64],
     # with BF16 subnormal and tiny inputs: forward bit-exact, gradient in tolerance
     edge = torch.tensor([2.0 ** -64, 2.0 ** -64 * (1 - 2 ** -24), 2.0 ** 64, 2.0 ** 64 * (1 + 2 ** -23),
@@ -254,6 +282,9 @@ def test_special_values():
         ref = oracle_grad(sp, xe, dye, edge, None)
         assert_grad_close(ds, ref["dscale"], ref["dscale_abs"])
         assert np.array_equal(dx, ref["dx"])
+        yf, dsf, _, dxf = gpu_fwd_grad(sp, xe, dye, edge, None)
+        assert np.array_equal(yf, y_ref) and np.array_equal(dxf, ref["dx"])
+        assert_grad_close(dsf, ref["dscale"], ref["dscale_abs"])
     sb = edge.repeat_interleave(4)                 # NVFP4: block scale = S_b / g * g
     for g in (1.0, 2.0 ** -30):
         ts = torch.tensor([g], dtype=torch.float32)
