@@ -9,26 +9,28 @@
 // One CTA computes up to MT = 4 output tiles of 128 x 128 of one expert that
 // share a column tile, K in steps of 64; the fake-quantized weight tile of a
 // step feeds all of them (the fake-quant work per FLOP falls by the number of
-// row tiles).  Warp w runs on scheduler w % 4; the MMA issuer shares its
-// scheduler with no fake-quant warp (arithmetic-heavy warps beside it starve
-// its issue slots and stall the tensor pipe):
+// row tiles).  Warp w runs on scheduler w % 4; the MMA issuer's scheduler
+// carries only the TMA warp and one fake-quant warp (arithmetic-heavy warps
+// beside it starve its issue slots and stall the tensor pipe):
 //   warp 1      allocates the 512 TMEM columns (4 FP32 accumulators of 128 x
 //               128); one lane issues tcgen05.mma (kind::f16, M=128, N=128,
-//               K=16; 4 K-slices x up to 4 row tiles per step) and commits
+//               K=16; up to 4 row tiles x 4 K-slices per step, tile by tile)
+//               and commits; it waits on its stages through try_wait
 //   warp 5      TMA producer: X tiles [128 rows, 64] -> shared (128-byte swizzle)
-//   warps 2-4, 6-8, 10, 11
-//               weight producers: load W chunks + block scales, fake-quantize
-//               them (the same chunk arithmetic as aqfq_qdq_fwd) and store the
-//               BF16 tile into shared memory in the 128-byte swizzle layout
+//   warps 0, 2-4, 6-12, 14-16, 18, 19 (16 warps, five on each scheduler but
+//               the MMA's)
+//               weight producers: each thread loads one 16-element W chunk
+//               and its block scale per step, fake-quantizes it (the same
+//               chunk arithmetic as aqfq_qdq_fwd) and stores the BF16 values
+//               into shared memory in the 128-byte swizzle layout
 //   warps 4-11  epilogue (TMEM -> registers -> BF16 -> Y), two warps per TMEM
-//               lane quarter (warp 0 sets up the barriers)
+//               lane quarter (warp 0 sets up the barriers first)
 // Two rings: X (2 stages of 4 tiles, 64 KiB each; full barriers count the TMA
 // bytes) and W_hat (4 stages of 16 KiB; one arrival per producer warp), so the
 // producers can run up to three k-steps ahead of the MMAs; empty barriers are
 // armed by tcgen05.commit.
 // Every CTA loads its own X tiles (column tiles of one row group read the
-// same X rows from L2; the loads are paced by each SM's intake of operand
-// bytes, not by L2).
+// same X rows from L2).
 // Every wait is bounded; on a timeout the CTA drains what it issued, frees
 // its tensor memory, raises the caller's error flag and returns.
 #include <cuda.h>
@@ -47,9 +49,11 @@ using namespace sm100;
 constexpr int BM = 128, BN = 128, BK = 64, MT = 4;
 constexpr int XS = 2;  // X ring stages (MT tiles of 16 KiB each)
 constexpr int WS = 4;  // fake-quantized weight ring stages (16 KiB each)
-constexpr int kGemmThreads = 384;  // 12 warps
+constexpr int kGemmThreads = 640;  // 20 warps
 constexpr int kMmaWarp = 1, kTmaWarp = 5;
-constexpr int kProducerThreads = 256;
+constexpr int kProducerThreads = 512;
+constexpr int kChunksPerProducer = BN * BK / 16 / kProducerThreads;  // 16-element chunks per thread and k-step
+static_assert(kChunksPerProducer * kProducerThreads * 16 == BN * BK, "producers cover the tile");
 constexpr uint32_t kTileBytes = BM * BK * 2;             // 16 KiB, one operand tile
 constexpr uint32_t kStageA = MT * kTileBytes;            // 64 KiB of X per stage
 constexpr uint32_t kTmemCols = MT * BN;                  // 512 columns
@@ -286,7 +290,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nt = blockIdx.x;
   const int KT = int(a.K / BK);
 
-  const bool producer = warp >= 2 && warp != kTmaWarp && warp != 9;
+  // producers: every warp but the MMA and TMA warps (1, 5, both on scheduler 1)
+  // and two idle ones (13, 17): 5 on each other scheduler and one beside the MMA
+  const bool producer = warp != kMmaWarp && warp != kTmaWarp && warp != 13 && warp != 17;
   if (warp == kTmaWarp) {
     // ---- TMA producer ----
     if (lane == 0) {
@@ -320,8 +326,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % XS, sw = kt % WS;
-        if (aborted(sh) || !mbar_wait(&sh->full_x[s], (kt / XS) & 1) ||
-            !mbar_wait(&sh->full_w[sw], (kt / WS) & 1)) {
+        if (aborted(sh) || !mbar_wait_suspend(&sh->full_x[s], (kt / XS) & 1) ||
+            !mbar_wait_suspend(&sh->full_w[sw], (kt / WS) & 1)) {
           set_abort(sh);
           ok = false;
           break;
@@ -330,13 +336,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t da = da0 + ((s * kStageA) >> 4), db = db0 + ((sw * kTileBytes) >> 4);
         // unrolled to MT with a guard: a loop bounded by the run-time tile
         // count issues the MMAs markedly slower
+        // tile by tile, each tile's four K-slices back to back (issuing two
+        // or three accumulators in turn measured up to twice as slow)
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
+        for (int i = 0; i < MT; ++i) {
+          if (i < ntiles) {
 #pragma unroll
-          for (int i = 0; i < MT; ++i)
-            if (i < ntiles)
+            for (int kk = 0; kk < BK / 16; ++kk)
               tc_mma_f16(tmem + uint32_t(i * BN), da + ((i * kTileBytes + kk * 32) >> 4),
                          db + ((kk * 32) >> 4), idesc, (kt | kk) != 0);
+          }
         }
         tc_commit(&sh->empty_x[s]);
         tc_commit(&sh->empty_w[sw]);
@@ -346,23 +355,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (producer) {
     // ---- weight producers (fake-quant into shared memory) ----
-    const int pw = warp - 2 - (warp > kTmaWarp ? 1 : 0) - (warp > 9 ? 1 : 0);  // 0..7
-    const int pt = pw * 32 + lane;                                              // 0..255
+    const int pw = warp - (warp > kMmaWarp) - (warp > kTmaWarp) - (warp > 13) - (warp > 17);  // 0..15
+    const int pt = pw * 32 + lane;                                                           // 0..511
     const int64_t kb = a.K / 16;
     const uint8_t* wrow = a.w + (size_t(e) * a.N + size_t(nt) * BN) * size_t(a.K) * 2;
     const float* srow = a.scale + (size_t(e) * a.N + size_t(nt) * BN) * size_t(kb);
-    int n_[2], j_[2];
+    int n_[kChunksPerProducer], j_[kChunksPerProducer];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kChunksPerProducer; ++i) {
       const int c = pt + i * kProducerThreads;
       n_[i] = c >> 2;
       j_[i] = c & 3;
     }
-    uint32_t xw[2][8];
-    float sbv[2];
+    uint32_t xw[kChunksPerProducer][8];
+    float sbv[kChunksPerProducer];
     // step 0's weights and block scales are in flight while the table is built
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kChunksPerProducer; ++i) {
       ld_stream(wrow + (size_t(n_[i]) * a.K + j_[i] * 16) * 2, xw[i]);
       sbv[i] = __ldg(srow + size_t(n_[i]) * kb + j_[i]);
     }
@@ -374,12 +383,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"n"(kProducerThreads) : "memory");
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % WS;
-      uint32_t nx[2][8];
-      float nsb[2];
+      uint32_t nx[kChunksPerProducer][8];
+      float nsb[kChunksPerProducer];
       const bool more = kt + 1 < KT;
       if (more) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kChunksPerProducer; ++i) {
           ld_stream(wrow + (size_t(n_[i]) * a.K + size_t(kt + 1) * BK + j_[i] * 16) * 2, nx[i]);
           nsb[i] = __ldg(srow + size_t(n_[i]) * kb + size_t(kt + 1) * (BK / 16) + j_[i]);
         }
@@ -396,13 +405,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       uint8_t* tile = tiles_b + s * kTileBytes;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) qdq_store_chunk(xw[i], sbv[i], g, rg, ng, stab, tile, n_[i], j_[i]);
+      for (int i = 0; i < kChunksPerProducer; ++i) qdq_store_chunk(xw[i], sbv[i], g, rg, ng, stab, tile, n_[i], j_[i]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->full_w[s]);
       if (more) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kChunksPerProducer; ++i) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) xw[i][q] = nx[i][q];
           sbv[i] = nsb[i];
@@ -410,7 +419,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   }
-  if (warp >= 4) {
+  if (warp >= 4 && warp < 12) {
     // ---- epilogue: TMEM lane quarter = warp % 4, two warps per quarter ----
     {
       bool ok = true;

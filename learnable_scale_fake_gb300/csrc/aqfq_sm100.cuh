@@ -62,6 +62,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// The same bounded wait through mbarrier.try_wait, which suspends the thread
+// in hardware until the phase completes (or a short system time limit passes)
+// instead of polling with a back-off: the thread resumes as soon as the phase
+// completes.  Gives up after about 2^31 clock cycles (~1 s) and returns false.
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+}
+
 // order generic-proxy shared-memory writes before async-proxy reads (tcgen05.mma)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
