@@ -41,6 +41,7 @@
 // order, to the rounding of the two normalisers.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "aqfq.h"
@@ -96,13 +97,16 @@ struct KdArgs {
 // thread count allows it.
 struct __align__(16) KdShared {
   uint64_t full[2];         // mbarriers of the two slice buffers
-  float xw[2][10];          // this CTA's reduction record (alternating exchange slots)
+  float xw[2][12];          // this CTA's reduction record (alternating exchange slots, 48 B each)
   float red[kWarps][9];     // per-warp records; per-warp loss sums in [w][0..1]
   int32_t ired[kWarps + 1];
   int32_t sel[8];           // threshold search results
   int32_t err;
   float res[10];            // the last reduction's result, for every thread
 };
+
+static_assert(offsetof(KdShared, xw) % 16 == 0 && sizeof(KdShared::xw[0]) % 16 == 0,
+              "exchange slots are read with 16-byte remote loads");
 
 // top-K only (dynamic shared memory after the histograms)
 struct __align__(16) TopkShared {
@@ -343,11 +347,12 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
   cluster_sync();
   if (w == 0) {
     Rec x = rec_empty();
-    if (l < kCl) {
+    if (l < kCl) {  // the record in two 16-byte loads and one word
       const uint32_t base = remote_addr(&sh->xw[par][0], uint32_t(l));
-      float v[9];
-#pragma unroll
-      for (int i = 0; i < 9; ++i) v[i] = ld_remote_f32(base + 4u * i);
+      const uint4 a0 = ld_remote_v4(base), a1 = ld_remote_v4(base + 16u);
+      const float v[9] = {__uint_as_float(a0.x), __uint_as_float(a0.y), __uint_as_float(a0.z),
+                          __uint_as_float(a0.w), __uint_as_float(a1.x), __uint_as_float(a1.y),
+                          __uint_as_float(a1.z), __uint_as_float(a1.w), ld_remote_f32(base + 32u)};
       x = rec_load(v);
     }
     if (k_before) {  // exclusive prefix over the ranks below this one
