@@ -358,6 +358,20 @@ aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void* teacher,
  * Asynchronous on `stream`; allocates nothing. */
 aqfq_status aqfq_selftest_wait_timeout(int32_t* flag, uint32_t polls, void* stream);
 
+/* Diagnostic (the pages have no counterpart): the grid rounding step of the
+ * fake-quant kernels applied to binary32 values given directly.  codes[i] is
+ * the code that the forward and gradient kernels give a quotient v[i]: INT8 /
+ * INT4 two's-complement codes of round-half-even(clamp(v, qmin, qmax)) (one
+ * byte per value; INT4 in the low nibble), E4M3 (spec->fmt = AQFQ_FP8_E4M3)
+ * bytes and E2M1 (AQFQ_NVFP4) nibbles of the saturating round-to-nearest-even
+ * conversion of |v| with the sign of v as the code's sign bit.  Lets a test
+ * compare that step with the oracle for every binary32 value.
+ *   spec   fmt and (INT) qmin / qmax as for the fake-quant calls
+ *   v      device float [n], 4-byte aligned;  codes  device uint8 [n]
+ * Asynchronous on `stream`; allocates nothing. */
+aqfq_status aqfq_selftest_grid_codes(const aqfq_qspec* spec, const float* v, int64_t n,
+                                     uint8_t* codes, void* stream);
+
 /* Static text for a status code. */
 const char* aqfq_status_string(aqfq_status status);
 

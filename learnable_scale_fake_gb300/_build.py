@@ -19,7 +19,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libaqfq.so")
 
 SOURCES = ["aqfq_api.cu", "aqfq_kernels.cu", "aqfq_fused.cu", "aqfq_stats.cu", "aqfq_noalloc.cu",
-           "aqfq_gemm.cu", "aqfq_kd.cu"]
+           "aqfq_gemm.cu", "aqfq_kd.cu", "aqfq_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division and denormals are part of the numerics contract: never fast math
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-prec-div=true",

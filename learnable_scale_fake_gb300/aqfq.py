@@ -32,7 +32,8 @@ EXPORTS = ("aqfq_qdq_fwd", "aqfq_grouped_qdq", "aqfq_grouped_qdq_gemm", "aqfq_sc
            "aqfq_qdq_fwd_grad", "aqfq_scale_grad_noalloc",
            "aqfq_scale_grad_workspace_bytes", "aqfq_observer_minmax", "aqfq_minmax_scale",
            "aqfq_scale_init", "aqfq_kd_loss", "aqfq_kd_workspace_bytes",
-           "aqfq_selftest_wait_timeout", "aqfq_status_string", "aqfq_version")
+           "aqfq_selftest_wait_timeout", "aqfq_selftest_grid_codes", "aqfq_status_string",
+           "aqfq_version")
 
 
 class QSpec(ctypes.Structure):
@@ -79,6 +80,7 @@ def lib():
                                        ctypes.c_float, P, P, P, P, P, sz, P]),
                 "aqfq_kd_workspace_bytes": (sz, [i64]),
                 "aqfq_selftest_wait_timeout": (i32, [P, ctypes.c_uint32, P]),
+                "aqfq_selftest_grid_codes": (i32, [S, P, i64, P, P]),
                 "aqfq_status_string": (ctypes.c_char_p, [i32]),
                 "aqfq_version": (i32, []),
             }
@@ -178,6 +180,17 @@ def aqfq_selftest_wait_timeout(flag, polls, stream=None):
         raise TypeError("flag must be int32")
     _check("aqfq_selftest_wait_timeout",
            lib().aqfq_selftest_wait_timeout(_ptr(flag), int(polls), _stream(stream)))
+
+
+def aqfq_selftest_grid_codes(spec, v, codes, stream=None):
+    """Diagnostic: the kernels' grid-rounding code of every binary32 value of v
+    (float32 device tensor) into codes (uint8, same length)."""
+    _f32(v, "v"), _u8(codes, "codes")
+    if codes.numel() != v.numel():
+        raise ValueError("codes must have one byte per value")
+    _check("aqfq_selftest_grid_codes",
+           lib().aqfq_selftest_grid_codes(ctypes.byref(spec), _ptr(v), v.numel(), _ptr(codes),
+                                          _stream(stream)))
 
 
 def aqfq_kd_workspace_bytes(T) -> int:

@@ -207,6 +207,17 @@ def test_observer_argument_checks(L):
     assert m(A, A + 2, 4, ctypes.c_float(448.0), A, None) == ALIGN
 
 
+def test_grid_codes_diagnostic_checks(L):
+    f = L.aqfq_selftest_grid_codes
+    assert f(None, A, 4, A, None) == NULL
+    assert f(ctypes.byref(I8), None, 4, A, None) == NULL
+    assert f(ctypes.byref(I8), A, -1, A, None) == SHAPE
+    assert f(ctypes.byref(I8), A + 2, 4, A, None) == ALIGN
+    assert f(ctypes.byref(aqfq.qspec(7, 0)), A, 4, A, None) == UNSUP
+    assert f(ctypes.byref(aqfq.qspec(aqfq.INT4, 0, qmin=-9, qmax=7)), A, 4, A, None) == UNSUP
+    assert f(ctypes.byref(I8), None, 0, None, None) == OK  # nothing to do
+
+
 def test_fastdiv_constants_exhaustive_small():
     """The host constants of the multiply-shift division (Granlund-Montgomery
     round-up method) reproduce n // d; checked here in Python for the divisors
