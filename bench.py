@@ -461,11 +461,17 @@ def main():
             wl.step(stream)
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, events per op and around the whole region ----
+    # ---- timed region: exactly K steps with no per-op events (a timing event
+    # between two short kernels costs ~1-2 us of device time), then K more
+    # steps with events around every op on the stream it is launched on, for
+    # the per-op times and the roofline ----
     nops = len(wl.ops)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(nops)] for _ in range(args.steps)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local)
     if dist is not None:
         dist.barrier()
@@ -475,13 +481,24 @@ def main():
     with torch.cuda.stream(stream):
         t0.record(stream)
         for k in range(args.steps):
+            if flush is not None:  # the flush stays outside the step's events
+                flush.fill_(k & 0xFF)
+                sev[k][0].record(stream)
+                wl.step(stream)
+                sev[k][1].record(stream)
+            else:
+                wl.step(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        i0.record(stream)
+        for k in range(args.steps):
             if flush is not None:
                 flush.fill_(k & 0xFF)
-            for i, op in enumerate(wl.ops):
-                ev[k][i][0].record(stream)
-                op.run(stream)
-                ev[k][i][1].record(stream)
-        t1.record(stream)
+            wl.step(stream, hook=lambda i, st, end, k=k: ev[k][i][int(end)].record(st))
+        i1.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     clk = clocks.stop(wall0, wall1)
@@ -490,8 +507,12 @@ def main():
     per_op = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
               for i in range(nops)]
     op_ms = [sum(v) / len(v) for v in per_op]
-    region_ms = t0.elapsed_time(t1)
-    step_ms = (sum(op_ms) if flush is not None else region_ms / args.steps)
+    if flush is None:
+        step_ms = t0.elapsed_time(t1) / args.steps
+        instr_ms = i0.elapsed_time(i1) / args.steps
+    else:
+        step_ms = sum(a.elapsed_time(b) for a, b in sev) / args.steps
+        instr_ms = sum(op_ms) if not wl.phases else None
     step_ms = max_over_ranks(step_ms, dist, device)
 
     bytes_step = wl.bytes_per_step  # FLOPs per step for a contraction workload
@@ -630,12 +651,17 @@ def main():
             "vs_baseline": None, "dtype": "f32", "storage": "bf16", "data": "synthetic",
             "config": dict(wl.config, l2=("flushed between steps (256 MiB write)" if small
                                           else "inputs larger than L2"),
-                           parallelism=f"replicas x{world}"),
+                           parallelism=f"replicas x{world}",
+                           **({"concurrent_phases": [[[wl.ops[i].name for i in lane] for lane in ph]
+                                                     for ph in wl.phases]} if wl.phases else {})),
             "gelem_per_s": round(gelem, 2),
             "pct_of_peak": round(100 * value / world / peak, 1),
             "pct_hbm_nominal_8tbs": (None if flops_kind else
                                      round(100 * value / world / NOMINAL_HBM_GBS, 1)),
             "per_op_ms": {op.name: round(op_ms[i], 4) for i, op in enumerate(wl.ops)},
+            "per_op_timing": ("CUDA events around each op on its own stream, in a second "
+                              f"region of {args.steps} steps"
+                              + (f"; that region's step {round(instr_ms, 4)} ms" if instr_ms else "")),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "unfused_path": unfused,
             "graph": graph,
             "gpu_launches": args.steps * sum(op.launches for op in wl.ops),

@@ -57,6 +57,8 @@ _lib = None
 def lib():
     """Load libaqfq.so (raises if it is missing: no CPU fallback exists)."""
     global _lib
+    if _lib is not None:  # loaded: no lock needed to read the reference
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):

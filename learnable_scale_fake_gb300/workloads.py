@@ -56,6 +56,12 @@ class Workload:
     ops: list = field(default_factory=list)
     inputs: dict = field(default_factory=dict)    # name -> device tensor a user uploads
     outputs: dict = field(default_factory=dict)   # name -> device tensor a user reads back
+    # None: the ops run in order on the caller's stream.  Otherwise a list of
+    # phases run one after another; a phase is a list of lanes (lists of op
+    # indices) that share no data and run concurrently, the first lane on the
+    # caller's stream, the others on side streams forked from it and joined
+    # back before the next phase.
+    phases: list | None = None
 
     @property
     def bytes_per_step(self) -> int:
@@ -65,9 +71,45 @@ class Workload:
     def elems_per_step(self) -> int:
         return sum(o.elems for o in self.ops)
 
-    def step(self, stream):
-        for o in self.ops:
-            o.run(stream)
+    def step(self, stream, hook=None):
+        """Launches one step on `stream`.  hook(i, st, end), if given, is called
+        on the stream st that runs op i, right before (end False) and right
+        after (end True) its launch."""
+        def one(i, st):
+            if hook is not None:
+                hook(i, st, False)
+            self.ops[i].run(st)
+            if hook is not None:
+                hook(i, st, True)
+
+        if not self.phases:
+            for i in range(len(self.ops)):
+                one(i, stream)
+            return
+        # every op launches on the stream it is given, so no current-stream
+        # switch is needed; lanes fork and join through events
+        # (an event may be recorded again once waited on: a wait takes the
+        # record made before it)
+        side, events = self._lanes(stream.device)
+        for phase, (fork, joins) in zip(self.phases, events):
+            fork.record(stream)
+            for st in side[:len(phase) - 1]:
+                st.wait_event(fork)
+            for st, lane in zip([stream] + side, phase):
+                for i in lane:
+                    one(i, st)
+            for st, join in zip(side[:len(phase) - 1], joins):
+                join.record(st)
+                stream.wait_event(join)
+
+    def _lanes(self, device):
+        """Side streams and the fork / join events of each phase (made once)."""
+        if "_lanes_made" not in self.__dict__:
+            n = max(len(ph) for ph in self.phases) - 1
+            side = [torch.cuda.Stream(device) for _ in range(n)]
+            events = [(torch.cuda.Event(), [torch.cuda.Event() for _ in ph[1:]]) for ph in self.phases]
+            self.__dict__["_lanes_made"] = (side, events)
+        return self.__dict__["_lanes_made"]
 
     # ---- end to end with host buffers -------------------------------------------
     def host_buffers(self):
@@ -250,6 +292,9 @@ def nvfp4_wa(dev, seed=0):
                                                      dx=dxa, workspace=ws, stream=st), 2))
     wl.inputs.update({"a": a, "dy_a": dya, "tscale_a": ga})
     wl.outputs.update({"y_a": ya, "dx_a": dxa, "dtscale_a": dga})
+    # the weight and the activation quantizers share no data: both forwards
+    # run concurrently, then both gradients
+    wl.phases = [[[0], [1]], [[2], [3]]]
     return wl
 
 
@@ -421,6 +466,7 @@ def nvfp4_wa_fused(dev, seed=0):
     _fused(wl, "a", spd, a, dya, None, ga, dx=torch.empty_like(a), ws=ws, dyn=True)
     wl.inputs.update({"w": w, "dy_w": dyw, "scale_w": s, "tscale_w": g, "a": a, "dy_a": dya,
                       "tscale_a": ga})
+    wl.phases = [[[0], [1]]]  # the two tensors' passes run concurrently
     return wl
 
 
