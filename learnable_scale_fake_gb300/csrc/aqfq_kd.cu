@@ -20,7 +20,9 @@
 // both rows in shared memory, brought in by two bulk copies (TMA, mbarrier)
 // issued as soon as the previous position has released the buffer, so HBM
 // sees each logit once and each gradient element once; the other CTAs of the
-// SM compute while one waits.  The row statistics (max and sum of
+// SM compute while one waits.  The top-K loss depends on the student only on
+// the support: its CTAs copy the teacher's slice alone and load the
+// student's vectors that hold support elements from device memory.  The row statistics (max and sum of
 // exponentials) and the top-K histograms are combined across the cluster
 // through distributed shared memory in a fixed order, so every CTA holds
 // bit-identical row values; each slice's loss sums go to the workspace and
@@ -523,7 +525,11 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
   uint16_t* vbin = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(tk) +
                                                (TOPK ? sizeof(TopkShared) : 0));  // bin of each vector max
   uint16_t* cand = vbin + nvb;                                                 // candidate vectors
-  uint16_t* buf0 = cand + nvb;  // kNbuf buffers of [teacher S | student S]
+  // kNbuf buffers of [teacher S | student S]; the top-K loss reads the
+  // student only on the support, from device memory, so its buffers hold the
+  // teacher's slice alone
+  uint16_t* buf0 = cand + nvb;
+  constexpr int kRows = TOPK ? 1 : 2;  // logit rows per buffer
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const int64_t v0 = int64_t(rank) * a.S;  // first vocabulary index of this slice
@@ -561,11 +567,11 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
     return -1;
   };
   auto prefetch = [&](int64_t r, int b) {  // thread 0
-    uint16_t* tb = buf0 + size_t(b) * 2 * a.S;
+    uint16_t* tb = buf0 + size_t(b) * kRows * a.S;
     if (bytes) {
-      sm100::mbar_arrive_expect_tx(&sh->full[b], 2u * bytes);
+      sm100::mbar_arrive_expect_tx(&sh->full[b], uint32_t(kRows) * bytes);
       bulk_load(tb, a.t + r * a.V + v0, bytes, &sh->full[b]);
-      bulk_load(tb + a.S, a.s + r * a.V + v0, bytes, &sh->full[b]);
+      if (!TOPK) bulk_load(tb + a.S, a.s + r * a.V + v0, bytes, &sh->full[b]);
     } else {
       sm100::mbar_arrive(&sh->full[b]);  // an empty slice completes the phase at once
     }
@@ -600,10 +606,13 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
     }
     if (!wait_phase(&sh->full[b], uses[b] & 1u)) atomicExch(&sh->err, 1);
     ++uses[b];
-    const uint16_t* tsl = buf0 + size_t(b) * 2 * a.S;
-    const uint16_t* ssl = tsl + a.S;
+    const uint16_t* tsl = buf0 + size_t(b) * kRows * a.S;
     const uint4* t4 = reinterpret_cast<const uint4*>(tsl);
-    const uint4* s4 = reinterpret_cast<const uint4*>(ssl);
+    // the student's 8-element vector v of this slice: shared memory, or (top-K
+    // support) device memory; rows and slices start on 16-byte boundaries
+    const uint4* s4 = reinterpret_cast<const uint4*>(tsl + a.S);
+    const uint4* s4g = reinterpret_cast<const uint4*>(a.s + row * a.V + v0);
+    auto svec = [&](int v) -> uint4 { return TOPK ? __ldg(s4g + v) : s4[v]; };
     const int64_t lloc = int64_t(a.labels[row]) - v0;  // the label's index within the slice
 
     // ---- pass 1: whole-vocabulary statistics (teacher; student unless TOPK) --
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
         uint4 x = make_uint4(0, 0, 0, 0);
         f2 SM = 0;
         if (!TOPK) {
-          x = s4[v];
+          x = svec(v);
           const float vs = vmax8(x);
           if (vs > smax) {
             const float f = ex2(__fmul_rn(__fsub_rn(smax, vs), ks));
@@ -807,7 +816,7 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
       for (int p = tid; p < nc; p += kThr) {
         const int v = cand[p];
         if (int(vbin[v]) < tbin) continue;
-        const uint4 w = t4[v], x = s4[v];
+        const uint4 w = t4[v], x = svec(v);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (!selected(8 * v + j, key_of(w, j))) continue;
@@ -854,7 +863,7 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
     // so it is formed from q = sum (p_s - p_t) d and the forward sum
     f2 fs2 = 0, q2 = 0;
     auto pass2_vector = [&](int v, bool masked) {
-      const uint4 w = t4[v], x = s4[v];
+      const uint4 w = t4[v], x = svec(v);
       uint32_t out[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -1063,8 +1072,9 @@ size_t ws_part_bytes(int64_t T) { return (size_t(T) * kCl * 8 + 255) / 256 * 256
 
 size_t kd_smem_bytes(int32_t S, bool topk) {
   const size_t vbin = topk ? size_t((S / 8 + 7) / 8 * 8) * 4 : 0;  // vector bins + candidate list
+  // each buffer: the teacher's slice, and the student's but for top-K
   return sizeof(KdShared) + (topk ? size_t(2 * kHistWords) * 4 + sizeof(TopkShared) : 0) + vbin +
-         size_t(S) * 4 * kNbuf;
+         size_t(S) * (topk ? 2 : 4) * kNbuf;
 }
 
 int max_smem_optin() {

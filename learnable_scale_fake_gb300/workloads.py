@@ -545,10 +545,13 @@ def _kd(name, kd_type, topk, dev, seed=0, T=synth.KD_TOKENS, V=synth.KD_VOCAB):
     label = {aqfq.KD_CAKLD: "cakld", aqfq.KD_KL: "kl", aqfq.KD_RKL: "rkl", aqfq.KD_MSE: "mse"}[kd_type]
     wl = Workload(name, f"distillation loss {label}{f' top-{topk}' if topk else ''}, logits [{T}, {V}]",
                   dict(CONFIGS[name], logits=[T, V]))
-    # algorithmic bytes: both logit rows read and the gradient row written at
-    # each valid position; only the (zero) gradient row at an ignored one
+    # algorithmic bytes: at each valid position both logit rows read and the
+    # gradient row written (top-K: the teacher row, the student's K support
+    # values and the gradient row); only the (zero) gradient row at an
+    # ignored one; the labels
     n_valid = int(((labels >= 0) & (labels < V)).sum())
-    nbytes = 6 * n_valid * V + 2 * (T - n_valid) * V + 4 * T
+    per_valid = (4 * V + 2 * topk) if topk else 6 * V
+    nbytes = per_valid * n_valid + 2 * (T - n_valid) * V + 4 * T
     wl.ops = [Op(f"kd_loss {label}", "kd_loss", n, nbytes,
                  lambda st: aqfq.aqfq_kd_loss(kd_type, student, teacher, labels, losses, ws, topk=topk,
                                               dstudent=ds, stream=st), launches=3)]
