@@ -309,12 +309,16 @@ __device__ __forceinline__ Rec rec_shfl(const Rec& a, int d) {
   return Rec{online_shfl(a.t, d), online_shfl(a.s, d), __shfl_xor_sync(0xFFFFFFFFu, a.u, d),
              __shfl_xor_sync(0xFFFFFFFFu, a.v, d), __shfl_xor_sync(0xFFFFFFFFu, a.k, d)};
 }
-// xor butterfly over the warp: every lane ends with the same total (the merge
-// is symmetric bit for bit), in a fixed order
-template <bool KMAX>
+// xor butterfly over the first N lanes (N a power of two, at most 32): each
+// of them ends with the same total (the merge is symmetric bit for bit), in a
+// fixed order.  Merging an empty record is exact (a scale of 2^0 = 1 and a
+// zero term), so with lanes N.. empty this gives the bits of the full
+// 32-lane butterfly in log2(N) steps.
+template <bool KMAX, int N = 32>
 __device__ __forceinline__ Rec warp_rec(Rec a, float ks) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "a power of two up to 32");
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) a = rec_merge<KMAX>(a, rec_shfl(a, d), ks);
+  for (int d = N / 2; d >= 1; d >>= 1) a = rec_merge<KMAX>(a, rec_shfl(a, d), ks);
   return a;
 }
 __device__ __forceinline__ void rec_store(float* p, const Rec& a) {
@@ -343,7 +347,7 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
   __syncthreads();
   if (w == 0) {
     Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
-    x = warp_rec<KMAX>(x, ks);
+    x = warp_rec<KMAX, kWarps>(x, ks);
     if (l == 0) rec_store(sh->xw[par], x);
   }
   cluster_sync();
@@ -366,7 +370,7 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
       }
       if (uint32_t(l) == cluster_rank()) sh->res[9] = __int_as_float(inc - x.k);
     }
-    x = warp_rec<KMAX>(x, ks);
+    x = warp_rec<KMAX, kCl>(x, ks);
     if (l == 0) rec_store(sh->res, x);
   }
   __syncthreads();
