@@ -63,6 +63,7 @@ using sm100::smem_u32;
 #endif
 constexpr int kCl = AQFQ_KD_CLUSTER;  // CTAs per position (vocabulary slices)
 constexpr int kNbuf = AQFQ_KD_NBUF;   // slice buffers per CTA
+static_assert(kNbuf == 1, "positions handed out one at a time use one slice buffer");
 #ifndef AQFQ_KD_THREADS
 #define AQFQ_KD_THREADS 256
 #endif
@@ -82,6 +83,8 @@ struct KdArgs {
   const uint16_t* t;        // teacher [T, V] BF16
   const int32_t* labels;    // [T]
   int32_t* ws_head;         // [0]: number of valid positions, [1]: error word
+  const int64_t* rows;      // [T]: the valid positions ascending, then the ignored ones
+  unsigned long long* ticket;  // the next position ticket (zeroed by the count kernel)
   float* part;              // workspace [T, kCl, 2]: each slice's forward / reverse KL sums
   float* rowx;              // workspace [T, 2]: conf and the sum of (s - t)^2 of each position
   uint16_t* ds;             // optional [T, V] BF16
@@ -99,7 +102,10 @@ struct KdArgs {
 // thread count allows it.
 struct __align__(16) KdShared {
   uint64_t full[2];         // mbarriers of the two slice buffers
-  float xw[2][12];          // this CTA's reduction record (alternating exchange slots, 48 B each)
+  unsigned long long tk0;   // rank 0: the cluster's first position ticket
+  unsigned long long tk;    // the ticket received in the last exchange that carried one
+  float xw[2][12];          // this CTA's reduction record (alternating exchange slots, 48 B
+                            // each; words 10-11: rank 0's next position ticket)
   float red[kWarps][9];     // per-warp records; per-warp loss sums in [w][0..1]
   int32_t ired[kWarps + 1];
   int32_t sel[8];           // threshold search results
@@ -125,16 +131,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
 // every thread of every CTA of the cluster; orders shared-memory writes before
 // the barrier with reads by any CTA after it
 __device__ __forceinline__ void cluster_sync() {
@@ -158,6 +154,12 @@ __device__ __forceinline__ uint4 ld_remote_v4(uint32_t a) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(a)
                : "memory");
+  return v;
+}
+// 8 bytes (two words) from an 8-byte aligned shared::cluster address
+__device__ __forceinline__ uint2 ld_remote_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
   return v;
 }
 __device__ __forceinline__ uint32_t ld_remote_u32(uint32_t a) {
@@ -335,20 +337,28 @@ __device__ __forceinline__ Rec rec_load(const float* p) {
 // of every CTA reads the kCl CTA records (lane r from rank r), merges them in
 // a fixed order and broadcasts the total through shared memory, so all CTAs
 // hold bit-identical totals.  k_before (if not NULL) receives the sum of k
-// over the ranks below this one.  A slot is rewritten two exchanges later,
+// over the ranks below this one.  With `tick` (not NULL) the exchange also
+// carries rank 0's *tick (next position ticket) to every CTA's *tick.  A slot is rewritten two exchanges later,
 // after a barrier that every CTA passes only once it has read the slot; the
 // warp records and the result are rewritten only after barriers that every
 // thread reaches after reading them.
 template <bool KMAX>
 __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par, float ks,
-                                           int* k_before = nullptr) {
+                                           int* k_before = nullptr,
+                                           unsigned long long* tick = nullptr) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) rec_store(sh->red[w], wr);
   __syncthreads();
   if (w == 0) {
     Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
     x = warp_rec<KMAX, kWarps>(x, ks);
-    if (l == 0) rec_store(sh->xw[par], x);
+    if (l == 0) {
+      rec_store(sh->xw[par], x);
+      if (tick) {
+        sh->xw[par][10] = __uint_as_float(uint32_t(*tick));
+        sh->xw[par][11] = __uint_as_float(uint32_t(*tick >> 32));
+      }
+    }
   }
   cluster_sync();
   if (w == 0) {
@@ -360,6 +370,10 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
                           __uint_as_float(a0.w), __uint_as_float(a1.x), __uint_as_float(a1.y),
                           __uint_as_float(a1.z), __uint_as_float(a1.w), ld_remote_f32(base + 32u)};
       x = rec_load(v);
+      if (tick && l == 0) {  // rank 0's ticket
+        const uint2 t = ld_remote_v2(base + 40u);
+        sh->tk = (static_cast<unsigned long long>(t.y) << 32) | t.x;
+      }
     }
     if (k_before) {  // exclusive prefix over the ranks below this one
       int inc = x.k;
@@ -376,6 +390,7 @@ __device__ __forceinline__ Rec cluster_rec(const Rec& wr, KdShared* sh, int& par
   __syncthreads();
   const Rec r = rec_load(sh->res);
   if (k_before) *k_before = __float_as_int(sh->res[9]);
+  if (tick) *tick = sh->tk;
   par ^= 1;
   return r;
 }
@@ -542,7 +557,6 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
   if (n64 < 0) n64 = 0;
   const int nvec = int(n64) >> 3;  // V % 8 == 0 and S % 8 == 0
   const uint32_t bytes = uint32_t(n64) * 2u;
-  const int64_t G = cluster_count();
   const int nval = a.ws_head[0];
   const float ks = a.ks;
   // d(tau^2 KL(s / tau)) / ds = tau dKL/db, over the mean
@@ -561,15 +575,6 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
   }
   __syncthreads();
 
-  auto is_valid = [&](int64_t r) {
-    const int32_t l = a.labels[r];
-    return l >= 0 && int64_t(l) < a.V;
-  };
-  auto next_valid = [&](int64_t r) -> int64_t {
-    for (; r < a.T; r += G)
-      if (is_valid(r)) return r;
-    return -1;
-  };
   auto prefetch = [&](int64_t r, int b) {  // thread 0
     uint16_t* tb = buf0 + size_t(b) * kRows * a.S;
     if (bytes) {
@@ -580,34 +585,29 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
       sm100::mbar_arrive(&sh->full[b]);  // an empty slice completes the phase at once
     }
   };
+  // Valid positions are handed out at run time, so that clusters on busier
+  // SMs take fewer: ticket t is the t-th valid position of the list.  Rank 0
+  // takes the cluster's next ticket while a position runs and passes it to
+  // its peers in that position's first exchange; the first one through a
+  // cluster barrier.  Every CTA of a cluster holds the same tickets.
+  if (tid == 0 && rank == 0) sh->tk0 = atomicAdd(a.ticket, 1ull);
+  cluster_sync();
+  unsigned long long tcur;
   {
-    const int64_t first = next_valid(cluster_id());
-    if (first >= 0 && tid == 0) prefetch(first, 0);
+    const uint2 t = ld_remote_v2(remote_addr(&sh->tk0, 0u));
+    tcur = (static_cast<unsigned long long>(t.y) << 32) | t.x;
   }
+  if (tid == 0 && tcur < (unsigned long long)nval) prefetch(a.rows[tcur], 0);
   uint32_t uses[2] = {0, 0};
   int it = 0, par = 0;
 
-  for (int64_t row = cluster_id(); row < a.T; row += G) {
+  while (tcur < (unsigned long long)nval) {
+    const int64_t row = a.rows[tcur];
+    unsigned long long tnext = 0;  // the next ticket: rank 0 takes it now
+    if (tid == 0 && rank == 0) tnext = atomicAdd(a.ticket, 1ull);
     uint16_t* drow = a.ds ? a.ds + row * a.V + v0 : nullptr;
-    if (!is_valid(row)) {  // the same decision in every CTA of the cluster: no exchange
-      if (drow)
-        for (int v = tid; v < nvec; v += kThr) st_stream16(drow + 8 * v, make_uint4(0, 0, 0, 0));
-      if (TOPK && rank == 0 && a.topk_idx)
-        for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
-      continue;
-    }
-    const int b = kNbuf == 2 ? (it & 1) : 0;
+    const int b = 0;
     ++it;
-    if (kNbuf == 2) {  // every read of the other buffer (the previous position) is done: refill it
-      __syncthreads();
-      if (tid == 0) {
-        const int64_t after = next_valid(row + G);
-        if (after >= 0) {
-          sm100::fence_proxy_async_smem();
-          prefetch(after, b ^ 1);
-        }
-      }
-    }
     if (!wait_phase(&sh->full[b], uses[b] & 1u)) atomicExch(&sh->err, 1);
     ++uses[b];
     const uint16_t* tsl = buf0 + size_t(b) * kRows * a.S;
@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
       for (int d = 16; d >= 1; d >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, d));
       wr.v = x;
     }
-    const Rec R1 = cluster_rec<true>(wr, sh, par, ks);
+    const Rec R1 = cluster_rec<true>(wr, sh, par, ks, nullptr, &tnext);
     const Online T_ = R1.t, S_ = R1.s;
     const float SE = R1.u, XL = R1.v;
     const int kmax = R1.k;
@@ -945,12 +945,9 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
         a.rowx[2 * row] = conf;
         a.rowx[2 * row + 1] = SE;
       }
-      if (kNbuf == 1) {  // one buffer: refill it
-        const int64_t after = next_valid(row + G);
-        if (after >= 0) {
-          sm100::fence_proxy_async_smem();
-          prefetch(after, 0);
-        }
+      if (tnext < (unsigned long long)nval) {  // the buffer is free: refill it
+        sm100::fence_proxy_async_smem();
+        prefetch(a.rows[tnext], 0);
       }
     }
     if (TOPK) {  // peers read these before the support-statistics exchange
@@ -958,6 +955,24 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
       if (tid < 16) tk->hist2[tid] = 0;
     }
     __syncthreads();
+    tcur = tnext;
+  }
+  // ignored positions: zero gradient slices (and -1 support indices); no
+  // exchange, so the (position, slice) pairs are spread over every CTA
+  {
+    const int64_t first = nval, npair = (a.T - first) * kCl;
+    for (int64_t p = blockIdx.x; p < npair; p += int64_t(gridDim.x)) {
+      const int64_t row = a.rows[first + p / kCl];
+      const int64_t vr0 = (p % kCl) * int64_t(a.S);
+      int64_t n = a.V - vr0;
+      if (n > a.S) n = a.S;
+      if (n < 0) n = 0;
+      if (a.ds)
+        for (int v = tid; v < int(n >> 3); v += kThr)
+          st_stream16(a.ds + row * a.V + vr0 + 8 * v, make_uint4(0, 0, 0, 0));
+      if (TOPK && p % kCl == 0 && a.topk_idx)
+        for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
+    }
   }
   // a copy whose wait timed out may still be landing: give it time before exit
   if (tid == 0 && sh->err) {
@@ -969,22 +984,46 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
   cluster_sync();
 }
 
-// number of positions whose label lies in [0, V); clears the error word and
-// the mean kernel's ticket
-__global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* head) {
+// Number of positions whose label lies in [0, V) (head[0]) and the list of
+// positions (rows): the valid ones ascending at [0, head[0]), the ignored ones
+// ascending after them; clears the error word, the mean kernel's ticket and
+// the loss kernel's position ticket.  One block.
+__global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* head,
+                                int64_t* rows) {
   __shared__ int part[32];
-  int c = 0;
-  for (int64_t i = threadIdx.x; i < T; i += blockDim.x) c += (labels[i] >= 0 && labels[i] < V);
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, d);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+  __shared__ int64_t base;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = int(blockDim.x >> 5);
+  if (threadIdx.x == 0) base = 0;
   __syncthreads();
+  for (int pass = 0; pass < 2; ++pass) {  // valid positions, then ignored ones
+    for (int64_t i0 = 0; i0 < T; i0 += blockDim.x) {
+      const int64_t i = i0 + threadIdx.x;
+      const bool valid = i < T && labels[i] >= 0 && labels[i] < V;
+      const int f = i < T && (valid == (pass == 0)) ? 1 : 0;
+      int x = f;  // block-wide inclusive scan of f
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+        if (lane >= d) x += y;
+      }
+      if (lane == 31) part[w] = x;
+      __syncthreads();
+      int before = 0, total = 0;
+      for (int k = 0; k < nw; ++k) {
+        if (k < w) before += part[k];
+        total += part[k];
+      }
+      if (f) rows[base + before + x - 1] = i;
+      __syncthreads();
+      if (threadIdx.x == 0) base += total;
+      __syncthreads();
+    }
+    if (pass == 0 && threadIdx.x == 0) head[0] = int(base);
+  }
   if (threadIdx.x == 0) {
-    int s = 0;
-    for (int k = 0; k < int(blockDim.x >> 5); ++k) s += part[k];
-    head[0] = s;
     head[1] = 0;
     head[2] = 0;  // the mean kernel's ticket
+    *reinterpret_cast<unsigned long long*>(head + 4) = 0ull;  // the loss kernel's position ticket
   }
 }
 
@@ -1067,8 +1106,9 @@ namespace {
 using namespace aqfq;
 
 // workspace: [0, 256) int32 valid count, error word and the mean kernel's
-// ticket; [256, 1024) the mean kernel's per-block double sums; then part
-// [T, kCl, 2] and rowx [T, 2] floats, each starting on a 256-byte boundary
+// ticket, at byte 16 the 64-bit position ticket; [256, 1024) the mean
+// kernel's per-block double sums; then part [T, kCl, 2] and rowx [T, 2]
+// floats and the position list [T] int64, each on a 256-byte boundary
 constexpr size_t kWsHead = 1024;
 constexpr size_t kWsBsum = 256;
 static_assert(kWsBsum + kMeanBlocks * 3 * sizeof(double) <= kWsHead, "block sums fit the head");
@@ -1126,7 +1166,7 @@ bool al(const void* p, uintptr_t b) { return (reinterpret_cast<uintptr_t>(p) & (
 
 extern "C" size_t aqfq_kd_workspace_bytes(int64_t T) {
   if (T < 0) return 0;
-  return kWsHead + ws_part_bytes(T) + (size_t(T) * 8 + 255) / 256 * 256;
+  return kWsHead + ws_part_bytes(T) + 2 * ((size_t(T) * 8 + 255) / 256 * 256);
 }
 
 extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void* teacher,
@@ -1158,7 +1198,8 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
   int32_t* head = static_cast<int32_t*>(workspace);
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead);
   float* rowx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead + ws_part_bytes(T));
-  kd_count_kernel<<<1, 1024, 0, st>>>(labels, T, V, head);
+  int64_t* rows = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(rowx) + (size_t(T) * 8 + 255) / 256 * 256);
+  kd_count_kernel<<<1, 1024, 0, st>>>(labels, T, V, head, rows);
   if (cudaGetLastError() != cudaSuccess) return AQFQ_ERR_CUDA;
   if (T > 0) {
     KdArgs a;
@@ -1166,6 +1207,8 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
     a.t = static_cast<const uint16_t*>(teacher);
     a.labels = labels;
     a.ws_head = head;
+    a.rows = rows;
+    a.ticket = reinterpret_cast<unsigned long long*>(head + 4);
     a.part = part;
     a.rowx = rowx;
     a.ds = static_cast<uint16_t*>(dstudent);
