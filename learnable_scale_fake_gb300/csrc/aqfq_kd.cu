@@ -986,41 +986,60 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
 
 // Number of positions whose label lies in [0, V) (head[0]) and the list of
 // positions (rows): the valid ones ascending at [0, head[0]), the ignored ones
-// ascending after them; clears the error word, the mean kernel's ticket and
-// the loss kernel's position ticket.  One block.
+// after them (filled from the end of the list); clears the error word, the
+// mean kernel's ticket and the loss kernel's position ticket.  One block, in
+// chunks of 4 rows per thread: one scan counts valid (low 16 bits) and
+// ignored (high 16 bits) rows together.
 __global__ void kd_count_kernel(const int32_t* labels, int64_t T, int64_t V, int32_t* head,
                                 int64_t* rows) {
   __shared__ int part[32];
-  __shared__ int64_t base;
+  __shared__ int64_t base_v, base_i;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = int(blockDim.x >> 5);
-  if (threadIdx.x == 0) base = 0;
+  if (threadIdx.x == 0) {
+    base_v = 0;
+    base_i = 0;
+  }
   __syncthreads();
-  for (int pass = 0; pass < 2; ++pass) {  // valid positions, then ignored ones
-    for (int64_t i0 = 0; i0 < T; i0 += blockDim.x) {
-      const int64_t i = i0 + threadIdx.x;
-      const bool valid = i < T && labels[i] >= 0 && labels[i] < V;
-      const int f = i < T && (valid == (pass == 0)) ? 1 : 0;
-      int x = f;  // block-wide inclusive scan of f
+  for (int64_t c0 = 0; c0 < T; c0 += int64_t(blockDim.x) * 4) {
+    const int64_t i0 = c0 + int64_t(threadIdx.x) * 4;
+    uint32_t fv = 0, fi = 0;  // bit j: row i0 + j valid / ignored
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
-        if (lane >= d) x += y;
+    for (int j = 0; j < 4; ++j)
+      if (i0 + j < T) {
+        const int32_t l = labels[i0 + j];
+        if (l >= 0 && int64_t(l) < V) fv |= 1u << j;
+        else fi |= 1u << j;
       }
-      if (lane == 31) part[w] = x;
-      __syncthreads();
-      int before = 0, total = 0;
-      for (int k = 0; k < nw; ++k) {
-        if (k < w) before += part[k];
-        total += part[k];
-      }
-      if (f) rows[base + before + x - 1] = i;
-      __syncthreads();
-      if (threadIdx.x == 0) base += total;
-      __syncthreads();
+    const int packed = __popc(fv) | (__popc(fi) << 16);  // a chunk has at most 4096 rows
+    int x = packed;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+      if (lane >= d) x += y;
     }
-    if (pass == 0 && threadIdx.x == 0) head[0] = int(base);
+    if (lane == 31) part[w] = x;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int k = 0; k < nw; ++k) {
+      if (k < w) before += part[k];
+      total += part[k];
+    }
+    const int ex = x - packed + before;
+    int64_t pv = base_v + (ex & 0xFFFF), pi = base_i + (ex >> 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((fv >> j) & 1u) rows[pv++] = i0 + j;
+      else if ((fi >> j) & 1u) rows[T - 1 - pi++] = i0 + j;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      base_v += total & 0xFFFF;
+      base_i += total >> 16;
+    }
+    __syncthreads();
   }
   if (threadIdx.x == 0) {
+    head[0] = int(base_v);
     head[1] = 0;
     head[2] = 0;  // the mean kernel's ticket
     *reinterpret_cast<unsigned long long*>(head + 4) = 0ull;  // the loss kernel's position ticket
