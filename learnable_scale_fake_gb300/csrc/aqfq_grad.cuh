@@ -300,18 +300,47 @@ __global__ void __launch_bounds__(kThreads) scale_grad_head_kernel(const HeadArg
   a.ws[j] = acc;
 }
 
-// dscale[h] = sum over r < used / cpt, c < cph of ws[r * cpt + h * cph + c]
-__global__ void reduce_heads_kernel(const double* ws, uint64_t rounds, uint32_t cpt, uint32_t cph,
-                                    int64_t H, float* out, int accumulate) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t h = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); h < H;
-       h += (int64_t)gridDim.x * (blockDim.x / 32)) {
+// dscale[h] = sum over r < used / cpt, c < cph of ws[r * cpt + h * cph + c]:
+// one block per head, thread t adding the head's partials i = t, t + blockDim,
+// ... (i = r cph + c, carried along without division), then the warps' sums
+// in warp order: a fixed order
+__global__ void __launch_bounds__(kThreads) reduce_heads_kernel(const double* ws, uint64_t rounds,
+                                                                uint32_t cpt, uint32_t cph,
+                                                                int64_t H, float* out,
+                                                                int accumulate) {
+  __shared__ double red[kThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint64_t n = rounds * cph;
+  const uint32_t dr = blockDim.x / cph, dc = blockDim.x % cph;
+  for (int64_t h = blockIdx.x; h < H; h += gridDim.x) {
     double t = 0.0;
-    const uint64_t n = rounds * cph;
-    for (uint64_t i = lane; i < n; i += 32) t += ws[(i / cph) * cpt + h * cph + (i % cph)];
+    uint64_t r = threadIdx.x / cph;
+    uint32_t c = threadIdx.x % cph;
+    for (uint64_t i0 = threadIdx.x; i0 < n; i0 += 8 * uint64_t(blockDim.x)) {
+      double v[8];  // eight loads in flight, then added in order
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = i0 + uint64_t(k) * blockDim.x < n ? ws[r * cpt + uint64_t(h) * cph + c] : 0.0;
+        r += dr;
+        c += dc;
+        if (c >= cph) {
+          c -= cph;
+          ++r;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t += v[k];
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-    if (lane == 0) store_grad(out + h, (float)t, accumulate);
+    if (lane == 0) red[w] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double sum = 0.0;
+      for (int k = 0; k < int(blockDim.x >> 5); ++k) sum += red[k];
+      store_grad(out + h, (float)sum, accumulate);
+    }
+    __syncthreads();
   }
 }
 
@@ -504,10 +533,10 @@ cudaError_t launch_head_grad(const Problem& p, const void* x, const void* dy, co
     case F_INT4: used = head_fmt<F_INT4, FWD>(p, a, st); break;
     default: used = head_fmt<F_FP8, FWD>(p, a, st); break;
   }
-  int64_t blocks = (p.rows + 7) / 8;
+  int64_t blocks = p.rows;  // one per head
   if (blocks > 65535) blocks = 65535;
-  reduce_heads_kernel<<<(unsigned)blocks, 256, 0, st>>>(ws, used / a.cpt, a.cpt, p.cpr, p.rows,
-                                                        dscale, accumulate);
+  reduce_heads_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(ws, used / a.cpt, a.cpt, p.cpr,
+                                                             p.rows, dscale, accumulate);
   return cudaGetLastError();
 }
 
