@@ -126,6 +126,16 @@ def test_many_positions_and_ignored_rows():
     check(O.KD_RKL, s, t, lab, topk=64, want_idx=True)
 
 
+def test_position_list_over_several_chunks():
+    """T = 9001 positions (the count kernel lists them in chunks of 4096, the
+    last one ragged), 30 % ignored, handed out by ticket to the clusters: every
+    position's loss and gradient row, and zero rows for the ignored ones."""
+    s, t, lab = synth.kd_logits(9001, 64, 31, ignore=0.3)
+    lab = lab.numpy()
+    check(O.KD_CAKLD, s, t, lab)
+    check(O.KD_KL, s, t, lab, topk=5, want_idx=True)
+
+
 def test_largest_vocabulary():
     """V = 262144 with the top-K histogram: the largest shared-memory layout."""
     s, t, lab = synth.kd_logits(3, 262144, 27)
