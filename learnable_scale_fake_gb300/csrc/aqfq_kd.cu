@@ -75,6 +75,7 @@ constexpr int kMinBlocks = AQFQ_KD_MINB;  // CTAs per SM the register budget is 
 constexpr int kWarps = kThr / 32;
 constexpr int kHist1 = 4096;    // bins: the top 12 bits of the 16-bit teacher key
 constexpr int kHistWords = kHist1 / 2;  // two 16-bit counters per word (a slice has < 2^16 elements)
+constexpr int kMaxPer = 256;  // top-K row kernel: vectors per thread, at most (V <= 2^19)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -495,6 +496,95 @@ __device__ __forceinline__ bool find_from_top(const uint32_t* hist, int top, int
   bin = 0;
   above = base;
   return false;
+}
+
+// Block reduction of one record per warp (`wr`: the warp's total, the same in
+// every lane): warp 0 merges the warps' records in warp order; every thread
+// receives the total.
+template <bool KMAX>
+__device__ __forceinline__ Rec block_rec(const Rec& wr, KdShared* sh, float ks) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) rec_store(sh->red[w], wr);
+  __syncthreads();
+  if (w == 0) {
+    Rec x = l < kWarps ? rec_load(sh->red[l]) : rec_empty();
+    x = warp_rec<KMAX, kWarps>(x, ks);
+    if (l == 0) rec_store(sh->res, x);
+  }
+  __syncthreads();
+  const Rec r = rec_load(sh->res);
+  __syncthreads();  // the records are rewritten by the next reduction
+  return r;
+}
+
+// Walking down from bin `top` of this CTA's 4096-bin histogram of 32-bit
+// counters: the bin at which the count reaches K and the count above it.
+// Warp 0 scans 256 bins per step (8 per lane); every thread receives the
+// result.  Returns false (bin 0, the whole count) when the histogram holds
+// fewer than K.  All threads call it.
+__device__ __forceinline__ bool find_local(const uint32_t* hist, int top, int K, int& bin,
+                                           int& above, KdShared* sh) {
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    int base = 0, found = 0, fb = 0, fa = 0;
+    for (int hi = top; hi >= 0 && !found; hi -= 256) {
+      uint32_t c[8];  // c[i]: bin hi - 8 l - i
+      int cl = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int b = hi - 8 * l - i;
+        c[i] = b >= 0 ? hist[b] : 0u;
+        cl += int(c[i]);
+      }
+      int x = cl;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+        if (l >= d) x += y;
+      }
+      const int incl = base + x;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, incl - cl < K && incl >= K);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        if (l == src) {
+          int run = incl - cl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run + int(c[i]) >= K) {
+              fb = hi - 8 * l - i;
+              fa = run;
+              break;
+            }
+            run += int(c[i]);
+          }
+        }
+        fb = __shfl_sync(0xFFFFFFFFu, fb, src);
+        fa = __shfl_sync(0xFFFFFFFFu, fa, src);
+        found = 1;
+      }
+      base = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (l == 0) {
+      sh->sel[1] = found;
+      sh->sel[6] = found ? fb : 0;
+      sh->sel[7] = found ? fa : base;
+    }
+  }
+  __syncthreads();
+  bin = sh->sel[6];
+  above = sh->sel[7];
+  const bool ok = sh->sel[1] != 0;
+  __syncthreads();  // sel is rewritten next
+  return ok;
+}
+
+// 16 bytes of a logit row from device memory (read-only for the kernel)
+__device__ __forceinline__ uint4 ld_row16(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 // Visits the vectors listed in cand[0..nc) (ascending vector indices) and calls
@@ -984,6 +1074,412 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_loss_kernel(const KdArgs 
   cluster_sync();
 }
 
+// ---------------------------------------------------------------------------
+// Top-K loss, one CTA per position
+// ---------------------------------------------------------------------------
+// The top-K loss and its gradient depend on the student only at the teacher's
+// K largest logits, so a position needs one read of the teacher row, the
+// student's values on the support and the gradient row (zeros outside the
+// support).  One CTA takes a whole position, with block barriers only:
+//   pass 1   the teacher row streamed once: the whole-vocabulary statistics
+//            (conf), the largest key, and the 12-bit bin of every 8-element
+//            vector maximum with their histogram (kept in shared memory)
+//   bound    the K-th largest vector maximum's bin bounds the K-th element
+//   exact    the elements of the candidate vectors (maximum at or above the
+//            bound, re-read, from L2) counted by key: exact 16-bit keys when
+//            they span at most 4096 of them, else 12-bit bins and then the
+//            low 4 bits of the threshold bin; the walk gives the threshold key
+//   ties     elements equal to it are taken in index order (each thread owns
+//            a contiguous range of vectors; one block scan)
+//   support  statistics of both distributions over the support, with the
+//            student's support vectors gathered from device memory
+//   pass 2   the gradient row: zeros outside the candidate vectors, the
+//            masked gradient in them; the loss sums
+// Positions are handed out by ticket as in kd_loss_kernel; the row's sums go
+// to slot 0 of the workspace's per-slice sums (the other slots hold zeros).
+template <bool RGRAD>
+__global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdArgs a) {
+  extern __shared__ __align__(16) uint8_t kd_smem[];
+  KdShared* sh = reinterpret_cast<KdShared*>(kd_smem);
+  uint32_t* vhist = reinterpret_cast<uint32_t*>(kd_smem + sizeof(KdShared));  // [4096] vector-max bins
+  uint32_t* hist1 = vhist + kHist1;                                            // [4096] element bins
+  uint32_t* hist2 = hist1 + kHist1;                                            // [16] low nibbles
+  uint16_t* vbin = reinterpret_cast<uint16_t*>(hist2 + 16);                    // [nvec] vector bins
+  constexpr int kHistAll = 2 * kHist1 + 16;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nvec = int(a.V >> 3);  // V % 8 == 0
+  const int vbin_bytes = (2 * nvec + 15) / 16 * 16;  // the bin array (16-byte multiple)
+  const int per = (nvec + kThr - 1) / kThr;  // this thread's contiguous vectors [c0, c1)
+  const int c0 = min(nvec, tid * per), c1 = min(nvec, c0 + per);
+  const int nval = a.ws_head[0];
+  const float ks = a.ks;
+  const float gsc = nval > 0 ? a.grad_scale * a.tau / float(nval) : 0.0f;
+  for (int i = tid; i < kHistAll; i += kThr) vhist[i] = 0u;
+  if (tid == 0) sh->tk = atomicAdd(a.ticket, 1ull);
+  __syncthreads();
+  unsigned long long tcur = sh->tk;
+  __syncthreads();
+
+  while (tcur < (unsigned long long)nval) {
+    const int64_t row = a.rows[tcur];
+    if (tid == 0) sh->tk = atomicAdd(a.ticket, 1ull);  // the next one, read at the end
+    const uint16_t* trow = a.t + row * a.V;
+    const uint16_t* srow = a.s + row * a.V;
+    uint16_t* drow = a.ds ? a.ds + row * a.V : nullptr;
+    const int64_t lab = a.labels[row];  // in [0, V): a valid position
+
+    // ---- pass 1: the teacher row ----------------------------------------------
+    float tmax = -INFINITY, xl = 0.0f;
+    f2 zt = 0;
+    {
+      const f2 KS = mk2(ks, ks);
+      for (int v0 = tid; v0 < nvec; v0 += 4 * kThr) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * kThr;
+          w[u] = v < nvec ? ld_row16(trow + 8 * int64_t(v)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * kThr;
+          if (v >= nvec) continue;
+          const float vt = vmax8(w[u]);
+          const uint32_t kb = key_of_f(vt) >> 4;
+          vbin[v] = uint16_t(kb);
+          atomicAdd(&vhist[kb], 1u);
+          if (vt > tmax) {
+            const float f = ex2(__fmul_rn(__fsub_rn(tmax, vt), ks));
+            zt = mul2(zt, mk2(f, f));
+            tmax = vt;
+          }
+          const f2 TM = mk2(tmax, tmax);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) zt = add2(zt, ex2x2(mul2(sub2(bf2(word(w[u], i)), TM), KS)));
+          if ((lab >> 3) == v) {  // the label's teacher logit
+            const int j = int(lab & 7);
+            xl = __uint_as_float(((word(w[u], j >> 1) >> ((j & 1) * 16)) & 0xFFFFu) << 16);
+          }
+        }
+      }
+    }
+    const Rec R1 = block_rec<true>(
+        warp_rec<true>(Rec{Online{tmax, __fadd_rn(lo2(zt), hi2(zt)), 0.0f}, online_empty(), 0.0f, xl,
+                           tmax > -INFINITY ? int(key_of_f(tmax)) : 0},
+                       ks),
+        sh, ks);
+    const Online T_ = R1.t;
+    const float conf = ex2(__fmaf_rn(__fsub_rn(R1.v, T_.m), ks, -log2f(T_.z)));
+    const int top = R1.k >> 4;
+
+    // ---- candidate vectors -------------------------------------------------------
+    int b0 = 0, above = 0;
+    if (!find_local(vhist, top, a.K, b0, above, sh)) b0 = 0;  // fewer than K vectors: all
+    // the vectors whose maximum is at or above the bound, ascending, written
+    // over the bins: each thread marks its range (at most 256 vectors) in a
+    // register mask before any thread writes
+    uint16_t* cand = vbin;
+    int nc;
+    {
+      uint32_t msk[kMaxPer / 32];
+      int cc = 0;
+#pragma unroll
+      for (int q = 0; q < kMaxPer / 32; ++q) {
+        uint32_t bits = 0;
+        const int n = min(32, (c1 - c0) - 32 * q);
+        for (int j = 0; j < n; ++j) bits |= (int(vbin[c0 + 32 * q + j]) >= b0 ? 1u : 0u) << j;
+        msk[q] = bits;
+        cc += __popc(bits);
+      }
+      int total;
+      int pos = block_scan(cc, total, sh) - cc;  // its barriers end every read of the bins
+#pragma unroll
+      for (int q = 0; q < kMaxPer / 32; ++q)
+        for (uint32_t bits = msk[q]; bits; bits &= bits - 1)
+          cand[pos++] = uint16_t(c0 + 32 * q + __ffs(bits) - 1);
+      nc = total;
+      __syncthreads();
+    }
+    // The candidates' teacher vectors are read from device memory once (the
+    // row has usually left L2 by now) and kept in the rest of the bin array,
+    // as many as fit; the later steps read them there.
+    uint4* tstage = reinterpret_cast<uint4*>(vbin) + (2 * nc + 15) / 16;
+    const int tcap = int((uint4*)(reinterpret_cast<uint8_t*>(vbin) + vbin_bytes) - tstage);
+    auto tvec = [&](int p, int v) {
+      return p < tcap ? tstage[p] : ld_row16(trow + 8 * int64_t(v));
+    };
+    // Candidate vectors are visited strided (every lane busy), four loads in
+    // flight: for_cand(f) calls f(v, w) for each candidate v with w its
+    // teacher vector (from device memory, staged on the way).
+    auto for_cand = [&](auto&& f) {
+      for (int p0 = tid; p0 < nc; p0 += 4 * kThr) {
+        uint4 w[4];
+        int v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int p = p0 + u * kThr;
+          v[u] = p < nc ? int(cand[p]) : -1;
+          w[u] = v[u] >= 0 ? ld_row16(trow + 8 * int64_t(v[u])) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v[u] >= 0) {
+            const int p = p0 + u * kThr;
+            if (p < tcap) tstage[p] = w[u];
+            f(v[u], w[u]);
+          }
+      }
+    };
+
+    // ---- threshold key -----------------------------------------------------------
+    const bool exact = (top - b0 + 1) * 16 <= kHist1;
+    const uint32_t kbase = uint32_t(b0) << 4;
+    for_cand([&](int, const uint4& w) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t k = key_of(w, j);
+        if (int(k >> 4) >= b0) atomicAdd(&hist1[exact ? k - kbase : (k >> 4)], 1u);
+      }
+    });
+    __syncthreads();
+    uint32_t tkey;
+    int need, eq_total;  // equal keys to take (index order), equal keys present
+    if (exact) {
+      int tb = 0;
+      find_local(hist1, int(((uint32_t(top) + 1u) << 4) - 1u - kbase), a.K, tb, above, sh);
+      tkey = kbase + uint32_t(tb);
+      need = a.K - above;
+      eq_total = int(hist1[tb]);
+    } else {
+      int bstar = 0;
+      find_local(hist1, top, a.K, bstar, above, sh);
+      for (int p = tid; p < nc; p += kThr) {
+        const uint4 w = tvec(p, int(cand[p]));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t k = key_of(w, j);
+          if (int(k >> 4) == bstar) atomicAdd(&hist2[k & 15u], 1u);
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        const int q = a.K - above;
+        int cum = 0, l = 15;
+        for (; l > 0; --l) {
+          if (cum + int(hist2[l]) >= q) break;
+          cum += int(hist2[l]);
+        }
+        sh->sel[2] = int((uint32_t(bstar) << 4) | uint32_t(l));
+        sh->sel[3] = q - cum;
+        sh->sel[4] = int(hist2[l]);
+      }
+      __syncthreads();
+      tkey = uint32_t(sh->sel[2]);
+      need = sh->sel[3];
+      eq_total = sh->sel[4];
+      __syncthreads();
+    }
+    const int tbin = int(tkey >> 4);
+    __syncthreads();  // every read of the histograms is done: the student stage reuses them
+
+    // ---- ties: the first `need` elements equal to the key, in index order ----
+    int idx_lim = 8 * nvec;  // every equal element taken
+    if (eq_total > need) {
+      if (tid == 0) sh->sel[5] = -1;
+      int base = 0;  // the same in every thread
+      for (int p0 = 0; p0 < nc && base < need; p0 += kThr) {
+        const int p = p0 + tid;
+        uint32_t em = 0;
+        int v = 0;
+        if (p < nc) {
+          v = cand[p];
+          const uint4 w = tvec(p, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) em |= (key_of(w, j) == tkey ? 1u : 0u) << j;
+        }
+        const int e = __popc(em);
+        int tot;
+        const int before = base + block_scan(e, tot, sh) - e;
+        if (before < need && before + e >= need) {  // the need-th is in this vector
+          uint32_t bits = em;
+          for (int k = before + 1; k < need; ++k) bits &= bits - 1;
+          sh->sel[5] = 8 * v + (__ffs(bits) - 1);
+        }
+        base += tot;
+      }
+      __syncthreads();
+      idx_lim = sh->sel[5];
+    }
+    auto selected = [&](int i, uint32_t k) { return k > tkey || (k == tkey && i <= idx_lim); };
+    // candidate vectors holding support elements: their maximum's bin reaches tbin
+    auto holds_support = [&](const uint4& w) { return int(key_of_f(vmax8(w)) >> 4) >= tbin; };
+
+    // ---- statistics over the support ---------------------------------------------
+    // each distribution as (raw maximum M, L = log2 of the sum of 2^((v - M) ks));
+    // the student's support vectors of the first 1024 candidates are kept in
+    // the element histogram (free once the key is known) for pass 2
+    uint4* sstage = reinterpret_cast<uint4*>(hist1);
+    constexpr int kScap = kHist1 * 4 / 16;
+    Online ut = online_empty(), us = online_empty();
+    int cnt = 0;
+    for (int p0 = tid; p0 < nc; p0 += 4 * kThr) {
+      uint4 w[4], x[4];
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + u * kThr;
+        v[u] = p < nc ? int(cand[p]) : -1;
+        w[u] = v[u] >= 0 ? tvec(p, v[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v[u] >= 0 && !holds_support(w[u])) v[u] = -1;
+        x[u] = v[u] >= 0 ? ld_row16(srow + 8 * int64_t(v[u])) : make_uint4(0, 0, 0, 0);
+        const int p = p0 + u * kThr;
+        if (v[u] >= 0 && p < kScap) sstage[p] = x[u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v[u] < 0) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (!selected(8 * v[u] + j, key_of(w[u], j))) continue;
+          const uint32_t tw = word(w[u], j >> 1), sw = word(x[u], j >> 1);
+          const float t = __uint_as_float(j & 1 ? tw & 0xFFFF0000u : tw << 16);
+          const float sv = __uint_as_float(j & 1 ? sw & 0xFFFF0000u : sw << 16);
+          ut = online_merge(ut, Online{t, 1.0f, 0.0f}, ks);
+          us = online_merge(us, Online{sv, 1.0f, __fmul_rn(__fsub_rn(sv, t), ks)}, ks);
+          ++cnt;
+        }
+      }
+    }
+    const Rec RS = block_rec<false>(warp_rec<false>(Rec{ut, us, 0.0f, 0.0f, cnt}, ks), sh, ks);
+    const float m_t = RS.t.m, m_s = RS.s.m, l_t = log2f(RS.t.z), l_s = log2f(RS.s.z);
+    const float bz = RS.s.b / RS.s.z;
+
+    // ---- pass 2: the gradient row and the loss sums ----------------------------
+    // zeros everywhere first; after a barrier the support's vectors over them
+    if (drow)
+      for (int v = tid; v < nvec; v += kThr)
+        st_stream16(drow + 8 * int64_t(v), make_uint4(0, 0, 0, 0));
+    __syncthreads();
+    const float dl = __fmaf_rn(__fsub_rn(m_t, m_s), ks, __fsub_rn(l_t, l_s));
+    const float rkl0 = kLn2 * (bz + dl);
+    const float wf = a.type == AQFQ_KD_KL ? 1.0f : a.type == AQFQ_KD_RKL ? 0.0f : 1.0f - conf;
+    const float wr2 = a.type == AQFQ_KD_KL ? 0.0f : a.type == AQFQ_KD_RKL ? 1.0f : conf;
+    const f2 KS = mk2(ks, ks), NLT = mk2(-l_t, -l_t), NLS = mk2(-l_s, -l_s);
+    const f2 MT = mk2(m_t, m_t), MS = mk2(m_s, m_s);
+    const float kl = ks * kLn2, ndl = -dl * kLn2;
+    const f2 KL2 = mk2(kl, kl), NDL = mk2(ndl, ndl);
+    const f2 WF = mk2(gsc * wf, gsc * wf), NWF = mk2(-gsc * wf, -gsc * wf);
+    const f2 NWR = mk2(-gsc * wr2, -gsc * wr2);
+    const float c = gsc * wf - gsc * wr2 * rkl0;
+    const f2 C2 = mk2(c, c);
+    f2 fs2 = 0, q2 = 0;
+    for (int p0 = tid; p0 < nc; p0 += 4 * kThr) {
+      uint4 w[4], x[4];
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + u * kThr;
+        v[u] = p < nc ? int(cand[p]) : -1;
+        w[u] = v[u] >= 0 ? tvec(p, v[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + u * kThr;
+        if (v[u] >= 0 && !holds_support(w[u])) v[u] = -1;
+        x[u] = v[u] < 0        ? make_uint4(0, 0, 0, 0)
+               : p < kScap ? sstage[p]
+                           : ld_row16(srow + 8 * int64_t(v[u]));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v[u] < 0) continue;
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const f2 t2 = bf2(word(w[u], i)), s2 = bf2(word(x[u], i));
+          f2 pt = ex2x2(fma2(sub2(t2, MT), KS, NLT)), ps = ex2x2(fma2(sub2(s2, MS), KS, NLS));
+          const bool in0 = selected(8 * v[u] + 2 * i, key_of(w[u], 2 * i));
+          const bool in1 = selected(8 * v[u] + 2 * i + 1, key_of(w[u], 2 * i + 1));
+          pt = mk2(in0 ? lo2(pt) : 0.0f, in1 ? hi2(pt) : 0.0f);
+          ps = mk2(in0 ? lo2(ps) : 0.0f, in1 ? hi2(ps) : 0.0f);
+          const f2 dn = fma2(sub2(t2, s2), KL2, NDL);  // log p_t - log p_s in nats
+          const f2 diff = sub2(ps, pt);
+          fs2 = add2(fs2, fma2(pt, dn, diff));
+          q2 = fma2(diff, dn, q2);
+          const f2 g = RGRAD ? fma2(ps, fma2(NWR, dn, C2), mul2(NWF, pt)) : mul2(WF, diff);
+          out[i] = pack2(g);
+        }
+        if (drow) st_stream16(drow + 8 * int64_t(v[u]), make_uint4(out[0], out[1], out[2], out[3]));
+      }
+    }
+    const f2 rs2 = sub2(mk2(0.0f, 0.0f), add2(q2, fs2));
+    {
+      float f = __fadd_rn(lo2(fs2), hi2(fs2)), r = __fadd_rn(lo2(rs2), hi2(rs2));
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) {
+        f = __fadd_rn(f, __shfl_xor_sync(0xFFFFFFFFu, f, d));
+        r = __fadd_rn(r, __shfl_xor_sync(0xFFFFFFFFu, r, d));
+      }
+      if (lane == 0) {
+        sh->red[tid >> 5][0] = f;
+        sh->red[tid >> 5][1] = r;
+      }
+    }
+    if (a.topk_idx) {  // the support in ascending vocabulary order (candidates are)
+      int32_t* out = a.topk_idx + row * a.K;
+      int base = 0;  // the same in every thread
+      for (int p0 = 0; p0 < nc; p0 += kThr) {
+        const int p = p0 + tid;
+        uint32_t sm8 = 0;
+        int v = 0;
+        if (p < nc) {
+          v = cand[p];
+          const uint4 w = tvec(p, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sm8 |= (selected(8 * v + j, key_of(w, j)) ? 1u : 0u) << j;
+        }
+        const int e = __popc(sm8);
+        int tot;
+        int pos = base + block_scan(e, tot, sh) - e;
+        for (uint32_t bits = sm8; bits; bits &= bits - 1) {
+          if (pos < a.K) out[pos] = 8 * v + __ffs(bits) - 1;
+          ++pos;
+        }
+        base += tot;
+      }
+    }
+    __syncthreads();  // every read of this row's candidates and sums is done
+    if (tid == 0) {
+      float F = 0.0f, R = 0.0f;
+      for (int k = 0; k < kWarps; ++k) {
+        F = __fadd_rn(F, sh->red[k][0]);
+        R = __fadd_rn(R, sh->red[k][1]);
+      }
+      a.part[row * kCl * 2] = F;
+      a.part[row * kCl * 2 + 1] = R;
+      a.rowx[2 * row] = conf;
+      a.rowx[2 * row + 1] = 0.0f;
+    }
+    if (tid >= 2 && tid < 2 * kCl) a.part[row * kCl * 2 + tid] = 0.0f;  // the other slots
+    for (int i = tid; i < kHistAll; i += kThr) vhist[i] = 0u;
+    const unsigned long long tnext = sh->tk;
+    __syncthreads();
+    tcur = tnext;
+  }
+  // ignored positions: zero gradient rows (and -1 support indices)
+  for (int64_t p = blockIdx.x; p < a.T - nval; p += int64_t(gridDim.x)) {
+    const int64_t row = a.rows[nval + p];
+    if (a.ds)
+      for (int v = tid; v < nvec; v += kThr)
+        st_stream16(a.ds + row * a.V + 8 * int64_t(v), make_uint4(0, 0, 0, 0));
+    if (a.topk_idx)
+      for (int j = tid; j < a.K; j += kThr) a.topk_idx[row * a.K + j] = -1;
+  }
+}
+
 // Number of positions whose label lies in [0, V) (head[0]) and the list of
 // positions (rows): the valid ones ascending at [0, head[0]), the ignored ones
 // after them (filled from the end of the list); clears the error word, the
@@ -1179,6 +1675,30 @@ cudaError_t launch_kd(const KdArgs& a, size_t smem, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// the top-K row kernel: bookkeeping, two 4096-bin histograms and the low
+// nibbles (32-bit counters), and the bin of every 8-element vector of a row
+size_t kd_row_smem_bytes(int64_t V) {
+  return sizeof(KdShared) + size_t(2 * kHist1 + 16) * 4 + (size_t(V / 8) * 2 + 15) / 16 * 16;
+}
+
+template <bool RGRAD>
+cudaError_t launch_kd_row(const KdArgs& a, size_t smem, cudaStream_t st) {
+  auto kern = kd_topk_row_kernel<RGRAD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThr, smem);
+  if (e != cudaSuccess) return e;
+  const int sms = aqfq::sm_count();
+  if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+  int64_t blocks = int64_t(per_sm) * sms;  // one wave, persistent over positions
+  if (blocks > a.T) blocks = a.T;
+  kern<<<unsigned(blocks), kThr, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 bool al(const void* p, uintptr_t b) { return (reinterpret_cast<uintptr_t>(p) & (b - 1)) == 0; }
 
 }  // namespace
@@ -1212,7 +1732,11 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
   const size_t smem = kd_smem_bytes(S, use_topk);
   const int optin = max_smem_optin();
   if (optin <= 0) return AQFQ_ERR_CUDA;
-  if (smem > size_t(optin)) return AQFQ_ERR_SHAPE;
+  // top-K: one CTA per position where its layout fits, else the cluster kernel
+  const size_t row_smem = kd_row_smem_bytes(V);
+  const bool row_path = use_topk && kd_type != AQFQ_KD_MSE && row_smem <= size_t(optin) &&
+                        V / 8 <= int64_t(kThr) * kMaxPer;
+  if (!row_path && smem > size_t(optin)) return AQFQ_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* head = static_cast<int32_t*>(workspace);
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead);
@@ -1244,6 +1768,8 @@ extern "C" aqfq_status aqfq_kd_loss(int kd_type, const void* student, const void
     const bool rgrad = dstudent && (kd_type == AQFQ_KD_RKL || kd_type == AQFQ_KD_CAKLD);
     cudaError_t e;
     if (kd_type == AQFQ_KD_MSE) e = launch_kd<false, false, true>(a, smem, st);
+    else if (row_path) e = rgrad ? launch_kd_row<true>(a, row_smem, st)
+                                 : launch_kd_row<false>(a, row_smem, st);
     else if (use_topk) e = rgrad ? launch_kd<true, true, false>(a, smem, st)
                                  : launch_kd<true, false, false>(a, smem, st);
     else e = rgrad ? launch_kd<false, true, false>(a, smem, st)
