@@ -1208,9 +1208,15 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdA
     auto tvec = [&](int p, int v) {
       return p < tcap ? tstage[p] : ld_row16(trow + 8 * int64_t(v));
     };
-    // Candidate vectors are visited strided (every lane busy), four loads in
-    // flight: for_cand(f) calls f(v, w) for each candidate v with w its
-    // teacher vector (from device memory, staged on the way).
+    // The student vectors of the first kPcap candidates are fetched along
+    // with them and kept in the vector-max histogram (free now); those of
+    // later candidates that hold support are fetched by the statistics and
+    // kept in the element histogram (free by then) for pass 2.
+    uint4* pstage = reinterpret_cast<uint4*>(vhist);
+    constexpr int kPcap = kHist1 * 4 / 16;
+    // Candidate vectors are visited strided (every lane busy), four per
+    // thread in flight: for_cand(f) calls f(v, w) for each candidate v with w
+    // its teacher vector (from device memory, staged on the way).
     auto for_cand = [&](auto&& f) {
       for (int p0 = tid; p0 < nc; p0 += 4 * kThr) {
         uint4 w[4];
@@ -1220,6 +1226,7 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdA
           const int p = p0 + u * kThr;
           v[u] = p < nc ? int(cand[p]) : -1;
           w[u] = v[u] >= 0 ? ld_row16(trow + 8 * int64_t(v[u])) : make_uint4(0, 0, 0, 0);
+          if (v[u] >= 0 && p < kPcap) pstage[p] = ld_row16(srow + 8 * int64_t(v[u]));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -1315,10 +1322,8 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdA
     auto holds_support = [&](const uint4& w) { return int(key_of_f(vmax8(w)) >> 4) >= tbin; };
 
     // ---- statistics over the support ---------------------------------------------
-    // each distribution as (raw maximum M, L = log2 of the sum of 2^((v - M) ks));
-    // the student's support vectors of the first 1024 candidates are kept in
-    // the element histogram (free once the key is known) for pass 2
-    uint4* sstage = reinterpret_cast<uint4*>(hist1);
+    // each distribution as (raw maximum M, L = log2 of the sum of 2^((v - M) ks))
+    uint4* sstage = reinterpret_cast<uint4*>(hist1) - kPcap;  // candidates kPcap ..
     constexpr int kScap = kHist1 * 4 / 16;
     Online ut = online_empty(), us = online_empty();
     int cnt = 0;
@@ -1333,10 +1338,12 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdA
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (v[u] >= 0 && !holds_support(w[u])) v[u] = -1;
-        x[u] = v[u] >= 0 ? ld_row16(srow + 8 * int64_t(v[u])) : make_uint4(0, 0, 0, 0);
         const int p = p0 + u * kThr;
-        if (v[u] >= 0 && p < kScap) sstage[p] = x[u];
+        if (v[u] >= 0 && !holds_support(w[u])) v[u] = -1;
+        x[u] = v[u] < 0     ? make_uint4(0, 0, 0, 0)
+               : p < kPcap ? pstage[p]
+                           : ld_row16(srow + 8 * int64_t(v[u]));
+        if (v[u] >= 0 && p >= kPcap && p < kPcap + kScap) sstage[p] = x[u];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -1389,9 +1396,10 @@ __global__ void __launch_bounds__(kThr, kMinBlocks) kd_topk_row_kernel(const KdA
       for (int u = 0; u < 4; ++u) {
         const int p = p0 + u * kThr;
         if (v[u] >= 0 && !holds_support(w[u])) v[u] = -1;
-        x[u] = v[u] < 0        ? make_uint4(0, 0, 0, 0)
-               : p < kScap ? sstage[p]
-                           : ld_row16(srow + 8 * int64_t(v[u]));
+        x[u] = v[u] < 0                 ? make_uint4(0, 0, 0, 0)
+               : p < kPcap             ? pstage[p]
+               : p < kPcap + kScap     ? sstage[p]
+                                       : ld_row16(srow + 8 * int64_t(v[u]));
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
