@@ -143,6 +143,14 @@ def test_largest_vocabulary():
     check(O.KD_KL, s, t, lab.numpy())
 
 
+def test_topk_beyond_the_row_kernel():
+    """V = 600000 (more than 2^16 vectors of 8): top-K takes the cluster kernel
+    (slices of the teacher row over 8 CTAs) instead of one CTA per position."""
+    s, t, lab = synth.kd_logits(3, 600000, 32)
+    check(O.KD_CAKLD, s, t, lab.numpy(), topk=1000, want_idx=True)
+    check(O.KD_KL, s, t, lab.numpy(), topk=7, want_idx=True)
+
+
 def test_no_valid_position_and_empty():
     s, t, lab = synth.kd_logits(4, 512, 28)
     lab = np.full(4, -100)
