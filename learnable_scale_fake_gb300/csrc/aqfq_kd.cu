@@ -20,13 +20,16 @@
 // both rows in shared memory, brought in by two bulk copies (TMA, mbarrier)
 // issued as soon as the previous position has released the buffer, so HBM
 // sees each logit once and each gradient element once; the other CTAs of the
-// SM compute while one waits.  The top-K loss depends on the student only on
-// the support: its CTAs copy the teacher's slice alone and load the
-// student's vectors that hold support elements from device memory.  The row statistics (max and sum of
+// SM compute while one waits.  The row statistics (max and sum of
 // exponentials) and the top-K histograms are combined across the cluster
 // through distributed shared memory in a fixed order, so every CTA holds
 // bit-identical row values; each slice's loss sums go to the workspace and
 // a second kernel adds them in rank order: results are reproducible.
+// The top-K loss depends on the student only on the support, and its
+// selection state fits one CTA: up to 2^19 vocabulary entries it runs one
+// CTA per position (kd_topk_row_kernel, block barriers only); beyond that in
+// the cluster kernel, whose CTAs then copy the teacher's slice alone and load
+// the student's vectors that hold support elements from device memory.
 //
 // Top-K support: 16-bit order-preserving keys of the teacher's BF16 values.
 // The K-th largest element is at least the K-th largest of the 8-element
