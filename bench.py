@@ -277,7 +277,14 @@ def oracle_run(name, inputs, k):
             t0 = time.perf_counter()
             O.kd_loss(kt, sb, tb, lab, topk=topk)
             secs += time.perf_counter() - t0
-            nbytes += int(bpe * tb.size)
+            # the workload's algorithmic bytes for these positions: both rows
+            # and the gradient row (top-K: the teacher row, K student values
+            # and the gradient row) per valid position, the zero gradient row
+            # per ignored one, the labels
+            V = tb.shape[1]
+            n_valid = int(((lab >= 0) & (lab < V)).sum())
+            per_valid = (4 * V + 2 * topk) if topk else 6 * V
+            nbytes += per_valid * n_valid + 2 * V * (kk - n_valid) + 4 * kk
             elems += tb.size
             continue
         xb = synth.bf16_bits(x[:kk])
