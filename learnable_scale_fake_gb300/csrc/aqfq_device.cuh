@@ -155,6 +155,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float hi, float lo) {
   return r;
 }
 
+// ---------------------------------------------------------------------------
+// Pairs of binary32 values in one 64-bit register (element 2i in the low
+// half) for the packed f32x2 instructions of sm_100-class GPUs.  Each lane is
+// rounded to nearest even as the scalar instruction rounds it (no flush of
+// subnormals), so a packed step gives the bits of two scalar steps.
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 mk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(f2 v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi2(f2 v) { return __uint_as_float(uint32_t(v >> 32)); }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// a BF16 pair (element 2i in the low half) as two binary32 values (exact)
+__device__ __forceinline__ f2 bf2(uint32_t w) { return mk2(bf_lo(w), bf_hi(w)); }
+// both lanes rounded to a BF16 pair, lane 0 in bits 15..0
+__device__ __forceinline__ uint32_t pack2(f2 v) { return pack_bf16x2(hi2(v), lo2(v)); }
+
 __device__ __forceinline__ float sign_zero(float x) {
   return __uint_as_float(__float_as_uint(x) & 0x80000000u);
 }
@@ -221,6 +260,22 @@ __device__ __forceinline__ float int_round(float v, const IntRange& r, uint32_t&
   float t = __fadd_rn(vc, kMagic);
   code = __float_as_uint(t);
   return __fsub_rn(t, kMagic);
+}
+
+// int_round of both lanes of a pair; t receives the biased sums (the codes in
+// their low bits)
+__device__ __forceinline__ f2 int_round2(f2 v, const IntRange& r, f2& t) {
+  const f2 kMagic = mk2(12582912.0f, 12582912.0f);  // 1.5 * 2^23
+  const f2 vc = mk2(fminf(fmaxf(lo2(v), r.qmin), r.qmax), fminf(fmaxf(hi2(v), r.qmin), r.qmax));
+  t = add2(vc, kMagic);
+  return sub2(t, kMagic);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t int_codes(f2 t) {
+  const uint32_t c0 = __float_as_uint(lo2(t)), c1 = __float_as_uint(hi2(t));
+  if constexpr (FMT == F_INT8) return (c0 & 0xFFu) | ((c1 & 0xFFu) << 8);
+  else return (c0 & 0xFu) | ((c1 & 0xFu) << 4);
 }
 
 template <int FMT>
@@ -397,6 +452,30 @@ __device__ __forceinline__ float mdiv(float x, const Divisor& d) {
   return __fmaf_rn(e, d.r, q0);
 }
 
+// mdiv of both lanes of a pair (q0 (-s) + x is the same exact value as
+// (-q0) s + x, so every lane has mdiv's bits)
+__device__ __forceinline__ f2 mdiv2(f2 x, const Divisor& d) {
+  const f2 r = mk2(d.r, d.r);
+  const f2 q0 = mul2(x, r);
+  const f2 e = fma2(q0, mk2(-d.s, -d.s), x);
+  return fma2(e, r, q0);
+}
+
+// The sum of a chunk's 2 NW gradient terms in one fixed order, shared by the
+// fast and the IEEE paths: a pairwise tree over the pairs, lane by lane (the
+// even elements' and the odd elements' totals), then their sum.  log2(2 NW)
+// levels of rounding, as a pairwise tree over the elements.
+template <int NW>
+__device__ __forceinline__ float chunk_sum(f2 (&t)[NW]) {
+  static_assert(NW >= 1 && (NW & (NW - 1)) == 0, "a power of two");
+#pragma unroll
+  for (int w = 1; w < NW; w *= 2) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2 * w) t[i] = add2(t[i], t[i + w]);
+  }
+  return __fadd_rn(lo2(t[0]), hi2(t[0]));
+}
+
 // ---------------------------------------------------------------------------
 // Fast-path chunks (Divisor::fast)
 // ---------------------------------------------------------------------------
@@ -417,23 +496,22 @@ __device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[NW], const D
                                                const IntRange& r, uint32_t (&yw)[NW],
                                                uint32_t (&cw)[4]) {
   if (CODES) cw[0] = cw[1] = cw[2] = cw[3] = 0;
+  const f2 S2 = mk2(d.s, d.s);
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
     uint32_t code = 0;
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
       // the integer grid maps +-0 alike (an integer code has no sign)
-      const float v0 = mdiv(bf_lo(xw[i]), d), v1 = mdiv(bf_hi(xw[i]), d);
-      float q0, q1;
-      bool k0, k1;
-      quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
-      yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s));
+      f2 t;
+      const f2 q = int_round2(mdiv2(bf2(xw[i]), d), r, t);
+      if (CODES) code = int_codes<FMT>(t);
+      yw[i] = pack2(mul2(q, S2));
     } else {
       // symmetric grid: round |v|, then give x's sign to the value and the code
-      const float a0 = mdiv(fabsf(bf_lo(xw[i])), d), a1 = mdiv(fabsf(bf_hi(xw[i])), d);
-      const uint32_t h = CODES ? fp_q2c<FMT>(a1, a0, code) : fp_q2<FMT>(a1, a0);
-      const float q0 = h2f((uint16_t)(h & 0xFFFFu)), q1 = h2f((uint16_t)(h >> 16));
+      const f2 a = mdiv2(bf2(xw[i] & 0x7FFF7FFFu), d);
+      const uint32_t h = CODES ? fp_q2c<FMT>(hi2(a), lo2(a), code) : fp_q2<FMT>(hi2(a), lo2(a));
       const uint32_t sgn = xw[i] & 0x80008000u;
-      yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s)) | sgn;
+      yw[i] = pack2(mul2(mk2(h2f((uint16_t)(h & 0xFFFFu)), h2f((uint16_t)(h >> 16))), S2)) | sgn;
       if (CODES) code |= code_signs<FMT>(sgn);
     }
     if (CODES) put_code<FMT>(cw, i, code);
@@ -446,43 +524,39 @@ template <int FMT, bool DX, bool FWD = false, int NW>
 __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
                                                  const Divisor& d, const IntRange& r,
                                                  uint32_t (&dxw)[NW], uint32_t* yw = nullptr) {
-  float t[2 * NW];
+  f2 t[NW];
+  const f2 S2 = mk2(d.s, d.s);
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
     // the sign of a zero quotient does not change a gradient term
-    const float v0 = mdiv(bf_lo(xw[i]), d), v1 = mdiv(bf_hi(xw[i]), d);
+    const f2 v = mdiv2(bf2(xw[i]), d);
+    const float v0 = lo2(v), v1 = hi2(v);
     bool k0, k1;
-    float term0, term1;
+    f2 term;
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
-      float q0, q1;
-      uint32_t code;
-      quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
-      term0 = k0 ? q0 : __fsub_rn(q0, v0);
-      term1 = k1 ? q1 : __fsub_rn(q1, v1);
-      if constexpr (FWD) yw[i] = pack_bf16x2(__fmul_rn(q1, d.s), __fmul_rn(q0, d.s));
+      f2 tb;
+      const f2 q = int_round2(v, r, tb);
+      k0 = (v0 <= r.qmin) || (v0 >= r.qmax);
+      k1 = (v1 <= r.qmin) || (v1 >= r.qmax);
+      const f2 dq = sub2(q, v);
+      term = mk2(k0 ? lo2(q) : lo2(dq), k1 ? hi2(q) : hi2(dq));
+      if constexpr (FWD) yw[i] = pack2(mul2(q, S2));
     } else {
       const uint32_t h = fp_q2<FMT>(v1, v0);
       k0 = fabsf(v0) >= grid_max<FMT>();
       k1 = fabsf(v1) >= grid_max<FMT>();
-      term0 = sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : v0);
-      term1 = sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : v1);
+      term = mk2(sub_h_f((uint16_t)(h & 0xFFFFu), k0 ? 0.0f : v0),
+                 sub_h_f((uint16_t)(h >> 16), k1 ? 0.0f : v1));
       if constexpr (FWD) {
         const uint32_t a = h & 0x7FFF7FFFu;  // |q| of the pair (f16)
-        yw[i] = pack_bf16x2(__fmul_rn(h2f((uint16_t)(a >> 16)), d.s),
-                            __fmul_rn(h2f((uint16_t)(a & 0xFFFFu)), d.s)) |
+        yw[i] = pack2(mul2(mk2(h2f((uint16_t)(a & 0xFFFFu)), h2f((uint16_t)(a >> 16))), S2)) |
                 (xw[i] & 0x80008000u);
       }
     }
-    t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
-    t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
+    t[i] = mul2(bf2(dw[i]), term);
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
-#pragma unroll
-  for (int w = 1; w < 2 * NW; w *= 2) {
-#pragma unroll
-    for (int i = 0; i < 2 * NW; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
-  }
-  return t[0];
+  return chunk_sum(t);
 }
 
 // ---------------------------------------------------------------------------
@@ -510,15 +584,15 @@ __device__ __forceinline__ void qdq_chunk(const uint32_t (&xw)[NW], float s, con
 
 // ---------------------------------------------------------------------------
 // One chunk, backward, IEEE division per element (as above):
-// returns sum_i dy_i * (clamped ? q_i : q_i - v_i), summed
-// pairwise in a fixed tree; optional STE mask of dy.  The term q - v is exact
+// returns sum_i dy_i * (clamped ? q_i : q_i - v_i), summed in chunk_sum's
+// fixed order; optional STE mask of dy.  The term q - v is exact
 // in binary32 (q and v are within a factor of two, Sterbenz), so the only
-// roundings are one per product and four levels of the tree.
+// roundings are one per product and four levels of the sum.
 // ---------------------------------------------------------------------------
 template <int FMT, bool DX, int NW>
 __device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
                                             float s, const IntRange& r, uint32_t (&dxw)[NW]) {
-  float t[2 * NW];
+  f2 t[NW];
   const bool zero = (s == 0.0f);
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
@@ -531,16 +605,10 @@ __device__ __forceinline__ float grad_chunk(const uint32_t (&xw)[NW], const uint
     quant_pair<FMT>(v0, v1, r, q0, q1, code, k0, k1);
     const float term0 = k0 ? q0 : __fsub_rn(q0, v0);
     const float term1 = k1 ? q1 : __fsub_rn(q1, v1);
-    t[2 * i] = __fmul_rn(bf_lo(dw[i]), term0);
-    t[2 * i + 1] = __fmul_rn(bf_hi(dw[i]), term1);
+    t[i] = mul2(bf2(dw[i]), mk2(term0, term1));
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
-#pragma unroll
-  for (int w = 1; w < 2 * NW; w *= 2) {
-#pragma unroll
-    for (int i = 0; i < 2 * NW; i += 2 * w) t[i] = __fadd_rn(t[i], t[i + w]);
-  }
-  return t[0];
+  return chunk_sum(t);
 }
 
 }  // namespace aqfq

@@ -146,26 +146,6 @@ __device__ void find_tile(const int32_t* off, int64_t E, int64_t total_m, int sl
 // division and dequantisation run as packed f32x2 operations (IEEE
 // round-to-nearest per lane, so every result is the scalar path's).
 
-// a pair of binary32 values in one 64-bit register (element 2i in the low half)
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 mk2(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float lo2(f2 v) { return __uint_as_float(uint32_t(v)); }
-__device__ __forceinline__ float hi2(f2 v) { return __uint_as_float(uint32_t(v >> 32)); }
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
 struct ScaleEntry {
   float s, r;  // S_hat and RN(1 / S_hat); r is NaN where the chunk takes the IEEE path
 };

@@ -38,7 +38,7 @@ template <int FMT, bool DYN, bool DX, int RED, bool FWD = false>
 struct GradTune {
   static constexpr bool heavy = DX || DYN || RED != 0;
   static constexpr int U = heavy ? 1 : (FWD || FMT == F_NVFP4 ? 2 : 3);
-  static constexpr int MINB = heavy ? 1 : (FWD ? 3 : (FMT == F_NVFP4 ? 5 : 4));
+  static constexpr int MINB = heavy ? (FWD ? 1 : 4) : (FWD ? 3 : (FMT == F_NVFP4 ? 5 : 4));
 };
 template <bool DX, bool FWD = false>
 struct RowTune {

@@ -182,47 +182,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // ---------------------------------------------------------------------------
-// arithmetic helpers; f2 = a pair of binary32 values in one 64-bit register
-// (packed FP32 instructions of sm_100-class GPUs)
+// arithmetic helpers (f2 pairs and their packed f32x2 operations come from
+// the device header)
 // ---------------------------------------------------------------------------
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 mk2(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float lo2(f2 v) { return __uint_as_float(uint32_t(v)); }
-__device__ __forceinline__ float hi2(f2 v) { return __uint_as_float(uint32_t(v >> 32)); }
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-  f2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
-  f2 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ f2 ex2x2(f2 v) { return mk2(ex2(lo2(v)), ex2(hi2(v))); }
-// a BF16 pair (element 2i in the low half) as two binary32 values
-__device__ __forceinline__ f2 bf2(uint32_t w) {
-  return mk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -232,11 +200,6 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float vmax8(uint4 w) {
   const uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
   return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint32_t pack2(f2 v) {  // RNE to a BF16 pair (lo in bits 15..0)
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi2(v)), "f"(lo2(v)));
-  return r;
 }
 // order-preserving 16-bit key of a BF16 value; -0 and +0 share a key
 __device__ __forceinline__ uint32_t okey(uint32_t b) {

@@ -69,6 +69,11 @@ CASES = [
     ("int8_tensor_k40", Q(aqfq.INT8, aqfq.PER_TENSOR, qmin=-128, qmax=127), (3, 17, 40),
      _x_normal, (1e-4, 4e-4), None),
     ("fp8_head_d24", Q(aqfq.FP8_E4M3, aqfq.PER_HEAD), (53, 5, 24), _x_normal, (2e-5, 2e-4), None),
+    # long rows: one CTA per row for the per-channel gradient (513 chunks of 8: a ragged tail)
+    ("fp8_channel_k4104", Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL), (1, 7, 4104), _x_normal,
+     (2e-5, 2e-4), None),
+    ("int8_channel_k4096", Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-128, qmax=127), (2, 5, 4096),
+     _x_normal, (1e-4, 4e-4), None),
 ]
 IDS = [c[0] for c in CASES]
 
@@ -148,7 +153,7 @@ def test_fused_forward_and_gradient(case):
 
 
 ACC = [c for c in CASES if c[0] in ("int8_channel_k512", "int4_g128", "fp8_tensor", "fp8_head",
-                                    "nvfp4_learned", "nvfp4_dynamic")]
+                                    "nvfp4_learned", "nvfp4_dynamic", "fp8_channel_k4104")]
 
 
 @pytest.mark.parametrize("case", ACC, ids=[c[0] for c in ACC])
