@@ -29,15 +29,18 @@ namespace {
 
 // Chunks per lane per iteration (U) and minimum resident CTAs per SM asked of
 // the register allocator (MINB), per kernel instantiation, from GB300 sweeps
-// on the workloads: more resident warps beat deeper per-lane unrolling for
-// the gradient until the register cap starts to spill, which the heavier
-// instantiations (STE input gradient, dynamic block scale, partial sums) do
-// (a cap of 4 CTAs per SM for them measured the same); the fused forward +
-// gradient (FWD) holds x_hat as well and runs best at U = 2, 3 CTAs per SM.
+// on the workloads: resident warps beat deeper per-lane unrolling once the
+// register cap makes the loop spill (INT4 group gradient of the expert stack:
+// U = 2 at 4 CTAs per SM 0.262 ms; U = 3 at 4, spilling, 0.270; U = 3 at 3,
+// 0.269).  The heavier instantiations (STE input gradient, dynamic block
+// scale, partial sums) take one chunk per lane and fit 64 registers, 4 CTAs
+// per SM, unfused; fused (FWD) they also hold x_hat and keep the allocator's
+// choice.  The fused forward + gradient otherwise runs best at U = 2, 3 CTAs
+// per SM.
 template <int FMT, bool DYN, bool DX, int RED, bool FWD = false>
 struct GradTune {
   static constexpr bool heavy = DX || DYN || RED != 0;
-  static constexpr int U = heavy ? 1 : (FWD || FMT == F_NVFP4 ? 2 : 3);
+  static constexpr int U = heavy ? 1 : 2;
   static constexpr int MINB = heavy ? (FWD ? 1 : 4) : (FWD ? 3 : (FMT == F_NVFP4 ? 5 : 4));
 };
 template <bool DX, bool FWD = false>
