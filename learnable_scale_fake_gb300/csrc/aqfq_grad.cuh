@@ -6,8 +6,9 @@
 // The gradient walks the chunks exactly as the forward does, recomputes v and
 // q, forms dy * (clamped ? q : q - v) per element and reduces it
 //   - per block / group (units of 16..512 elements = 1..32 aligned lanes):
-//     pairwise tree in the lane, xor-butterfly across the unit's lanes, one
-//     store per unit (no atomics, no workspace);
+//     the chunk's fixed-order sum in the lane (chunk_sum), xor-butterfly
+//     across the unit's lanes, one store per unit (no atomics, no
+//     workspace);
 //   - per channel with long rows: one warp per row, per-lane double
 //     accumulation of chunk sums, double butterfly;
 //   - per tensor / NVFP4 tensor scale: per-CTA double partials into the
