@@ -249,7 +249,36 @@ __device__ __forceinline__ float2 dec_e2m1x2(uint32_t c) {
 // ---------------------------------------------------------------------------
 struct IntRange {
   float qmin, qmax;
+  // With `centred`, c = (qmin + qmax) / 2 and h = (qmax - qmin) / 2 decide
+  // the clamp in one comparison: |RN(v - c)| >= h exactly when v <= qmin or
+  // v >= qmax, for every binary32 v (NaN: neither).  The forward ignores them.
+  float c = 0.0f, h = 0.0f;
+  bool centred = false;
 };
+
+// An integer grid [qmin, qmax] (integers, qmin < qmax) with its one-compare
+// clamp test where that test is exact: c = 0, or c = -1/2 with qmax not a
+// power of two, or c = +1/2 with -qmin not a power of two, and h >= 1.
+// v - c is then exact wherever it lies within rounding distance of h (it
+// lands in v's binade or a finer one); with c = -1/2 and qmax = 2^k, v just
+// below qmax has a finer ulp than v + 1/2, which can round up onto h (qmax = 1,
+// v = 1 - 2^-24).  Checked against the two comparisons on all 2^32 binary32
+// values for [-8,7], [-128,127], [-127,127], [-7,7], [-4,3], [-3,4], [-16,16]
+// (and the two excluded cases [-2,1], [-1,2], one mismatch each).
+inline IntRange int_range(float qmin, float qmax) {
+  IntRange r;
+  r.qmin = qmin;
+  r.qmax = qmax;
+  r.c = 0.5f * (qmin + qmax);  // exact: integers of magnitude <= 2^22
+  r.h = 0.5f * (qmax - qmin);
+  auto pow2 = [](float x) {
+    const long long q = (long long)x;
+    return x >= 1.0f && float(q) == x && (q & (q - 1)) == 0;
+  };
+  const bool ok = r.c == 0.0f || (r.c == -0.5f && !pow2(qmax)) || (r.c == 0.5f && !pow2(-qmin));
+  r.centred = ok && r.h >= 1.0f;
+  return r;
+}
 
 // clamp then round half to even via t = vc + 1.5*2^23 (|vc| <= 128 << 2^22):
 // t's low bits hold the integer in two's complement; t - 1.5*2^23 is the
@@ -519,11 +548,13 @@ __device__ __forceinline__ void qdq_chunk_fast(const uint32_t (&xw)[NW], const D
 }
 
 // FWD: also the forward's x_hat of the chunk into yw (the same bits as
-// qdq_chunk_fast: FP grids give |q| * s the sign of x, so -0 stays -0)
-template <int FMT, bool DX, bool FWD = false, int NW>
-__device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
-                                                 const Divisor& d, const IntRange& r,
-                                                 uint32_t (&dxw)[NW], uint32_t* yw = nullptr) {
+// qdq_chunk_fast: FP grids give |q| * s the sign of x, so -0 stays -0).
+// CENT: integer grids decide the clamp by |v - c| >= h (IntRange::centred).
+template <int FMT, bool DX, bool FWD, bool CENT, int NW>
+__device__ __forceinline__ float grad_chunk_fast_impl(const uint32_t (&xw)[NW],
+                                                      const uint32_t (&dw)[NW], const Divisor& d,
+                                                      const IntRange& r, uint32_t (&dxw)[NW],
+                                                      uint32_t* yw) {
   f2 t[NW];
   const f2 S2 = mk2(d.s, d.s);
 #pragma unroll
@@ -536,8 +567,14 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const
     if constexpr (FMT == F_INT8 || FMT == F_INT4) {
       f2 tb;
       const f2 q = int_round2(v, r, tb);
-      k0 = (v0 <= r.qmin) || (v0 >= r.qmax);
-      k1 = (v1 <= r.qmin) || (v1 >= r.qmax);
+      if constexpr (CENT) {
+        const f2 vc = sub2(v, mk2(r.c, r.c));
+        k0 = fabsf(lo2(vc)) >= r.h;
+        k1 = fabsf(hi2(vc)) >= r.h;
+      } else {
+        k0 = (v0 <= r.qmin) || (v0 >= r.qmax);
+        k1 = (v1 <= r.qmin) || (v1 >= r.qmax);
+      }
       const f2 dq = sub2(q, v);
       term = mk2(k0 ? lo2(q) : lo2(dq), k1 ? hi2(q) : hi2(dq));
       if constexpr (FWD) yw[i] = pack2(mul2(q, S2));
@@ -557,6 +594,16 @@ __device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const
     if (DX) dxw[i] = (k0 ? 0u : (dw[i] & 0xFFFFu)) | (k1 ? 0u : (dw[i] & 0xFFFF0000u));
   }
   return chunk_sum(t);
+}
+
+template <int FMT, bool DX, bool FWD = false, int NW>
+__device__ __forceinline__ float grad_chunk_fast(const uint32_t (&xw)[NW], const uint32_t (&dw)[NW],
+                                                 const Divisor& d, const IntRange& r,
+                                                 uint32_t (&dxw)[NW], uint32_t* yw = nullptr) {
+  if constexpr (FMT == F_INT8 || FMT == F_INT4) {
+    if (r.centred) return grad_chunk_fast_impl<FMT, DX, FWD, true>(xw, dw, d, r, dxw, yw);
+  }
+  return grad_chunk_fast_impl<FMT, DX, FWD, false>(xw, dw, d, r, dxw, yw);
 }
 
 // ---------------------------------------------------------------------------

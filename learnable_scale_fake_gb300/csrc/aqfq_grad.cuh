@@ -530,7 +530,7 @@ cudaError_t launch_head_grad(const Problem& p, const void* x, const void* dy, co
   a.nchunks = uint64_t(p.batch) * a.cpt;
   a.cph = make_fastdiv(p.cpr);
   a.used = 0;
-  a.ir = IntRange{p.qmin, p.qmax};
+  a.ir = int_range(p.qmin, p.qmax);
   uint64_t used;
   switch (p.fmt) {
     case F_INT8: used = head_fmt<F_INT8, FWD>(p, a, st); break;
@@ -582,7 +582,7 @@ cudaError_t launch_grad(const Problem& p, const void* x, const void* dy, const f
   a.cpb = p.cpb;
   a.cpr = make_fastdiv(p.cpr);
   a.lg = grad_unit_lg(p);
-  a.ir = IntRange{p.qmin, p.qmax};
+  a.ir = int_range(p.qmin, p.qmax);
   a.accumulate = accumulate;
   a.nparts = 0;
   if (partials) {  // the ticket starts at zero on the stream, before the kernel
