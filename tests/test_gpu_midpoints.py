@@ -149,6 +149,14 @@ CASES = [
     ("int8_channel_row_kernel", INT8, ("int", 127), "channel", 48),
     ("int4_g16", Q(aqfq.INT4, aqfq.PER_GROUP, group=16, qmin=-8, qmax=7), ("int", 7), "channel", 16),
     ("int4_g128", Q(aqfq.INT4, aqfq.PER_GROUP, group=128, qmin=-8, qmax=7), ("int", 7), "channel", 128),
+    # grids whose one-comparison clamp test is exact (centre -1/2, +1/2) and
+    # grids where it is not and the two comparisons stay (qmax or -qmin a power
+    # of two: the quotient one ulp inside it, e.g. 1 - 2^-24, is a target)
+    ("int4_g16_m4_3", Q(aqfq.INT4, aqfq.PER_GROUP, group=16, qmin=-4, qmax=3), ("int", 3), "channel", 16),
+    ("int4_g16_m3_4", Q(aqfq.INT4, aqfq.PER_GROUP, group=16, qmin=-3, qmax=4), ("int", 3), "channel", 16),
+    ("int4_g16_m2_1", Q(aqfq.INT4, aqfq.PER_GROUP, group=16, qmin=-2, qmax=1), ("int", 1), "channel", 16),
+    ("int4_g16_m1_2", Q(aqfq.INT4, aqfq.PER_GROUP, group=16, qmin=-1, qmax=2), ("int", 1), "channel", 16),
+    ("int8_channel_m65_64", Q(aqfq.INT8, aqfq.PER_CHANNEL, qmin=-65, qmax=64), ("int", 64), "channel", 16),
     ("fp8_channel", Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL), ("e4m3",), "channel", 16),
     ("fp8_channel_row_kernel", Q(aqfq.FP8_E4M3, aqfq.PER_CHANNEL), ("e4m3",), "channel", 48),
     ("fp8_tensor", Q(aqfq.FP8_E4M3, aqfq.PER_TENSOR), ("e4m3",), "tensor", 16),
